@@ -1,0 +1,123 @@
+"""Oracle: tree-verify attention, computed literally per root path in fp64.
+
+Test infrastructure only (see the package docstring).
+
+Definition followed ([AK] section one, "Target Verify" identity; [MI] "Here is
+the problem trees solve"): the verify row of node v must equal the target's
+attention over the committed prefix followed by v's own root path,
+L(v) = Target(prefix + path(root -> v)).
+
+For request b with committed prefix length P (= vc), node v with root path
+u_0 = 0, ..., u_D = v, and query head h reading KV head h // (Hq / Hkv):
+
+  keys   = [K_cache(b, p) for p < P] ++ [RoPE(k_new[u_t], P + t) for t = 0..D]
+  values = [V_cache(b, p) for p < P] ++ [v_new[u_t]                for t = 0..D]
+  q      = RoPE(q_raw[v, h], P + D)
+  s      = (q . keys) * scale,         scale = 1/sqrt(d) unless given
+  out    = softmax(s) . values
+  lse2   = ln(sum exp(s)) / ln 2       (base-2 log-sum-exp, [TS] "One tree attention")
+
+The prefix keys in the cache are already rotated (their positions are p < P).
+Window node u_t sits at logical position P + t because its depth is t
+([TS] "Position follows depth"); slot follows node index, so the oracle takes
+window K/V from k_new/v_new by node index and never reads the mask, the
+positions array or the cache's window slots.
+
+Readings taken where the pages are silent: scale 1/sqrt(d); query head h reads
+KV head h // (Hq/Hkv); RoPE is the rotate-half form (oracle.rope).
+
+The prefix scores of many nodes are formed with one matrix product per KV
+head (the same dot products, batched); each node's softmax is then taken over
+its own concatenated key list.
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, Optional
+
+import numpy as np
+
+from . import rope
+from .tree import root_path
+
+LN2 = math.log(2.0)
+
+
+def widen(a) -> np.ndarray:
+    """bf16 bits (uint16) -> fp64 exactly; float arrays -> fp64."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def prefix_slots(page_table_row, P: int, page_size: int) -> np.ndarray:
+    pos = np.arange(P, dtype=np.int64)
+    return np.asarray(page_table_row, dtype=np.int64)[pos // page_size] * page_size + pos % page_size
+
+
+def verify_attention(q, k_new, v_new, k_cache, v_cache, page_table, prefix_len, parents,
+                     Hkv: int, theta: float, page_size: int = 64, scale: Optional[float] = None,
+                     rows: Optional[Iterable] = None, q_rotated: bool = False,
+                     max_chunk_elems: int = 1 << 24):
+    """Returns (out [B*N][Hq][d] fp64, lse2 [B*N][Hq] fp64).
+
+    q: [B*N][Hq][d]; k_new, v_new: [B*N][Hkv][d]; k_cache, v_cache:
+    [slots][Hkv][d] (bf16 bits or floats); page_table int [B][max_pages];
+    prefix_len int [B]; parents int [B][N]. ``rows`` restricts the work to the
+    given (b, v) pairs; the other rows are NaN. ``q_rotated`` skips the query
+    rotation (the caller passes already-rotated queries).
+    """
+    parents = np.asarray(parents)
+    B, N = parents.shape
+    q = np.asarray(q)
+    Hq, d = q.shape[1], q.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = np.full((B * N, Hq, d), np.nan)
+    lse2 = np.full((B * N, Hq), np.nan)
+    if rows is None:
+        want = {b: list(range(N)) for b in range(B)}
+    else:
+        want = {}
+        for b, v in rows:
+            want.setdefault(int(b), []).append(int(v))
+
+    for b, nodes in sorted(want.items()):
+        P = int(prefix_len[b])
+        slots = prefix_slots(page_table[b], P, page_size)
+        Kp = np.ascontiguousarray(widen(np.asarray(k_cache)[slots]).transpose(1, 0, 2))  # [Hkv][P][d]
+        Vp = np.ascontiguousarray(widen(np.asarray(v_cache)[slots]).transpose(1, 0, 2))
+
+        # per node: its path, rotated query, rotated window keys
+        info = []
+        for v in nodes:
+            path = root_path(parents[b], v)
+            D = len(path) - 1
+            rows_bn = [b * N + u for u in path]
+            kw = rope.rotate(widen(np.asarray(k_new)[rows_bn]), P + np.arange(D + 1)[:, None], theta)
+            vw = widen(np.asarray(v_new)[rows_bn])                      # [D+1][Hkv][d]
+            qv = widen(q[b * N + v])
+            if not q_rotated:
+                qv = rope.rotate(qv, P + D, theta)                      # [Hq][d]
+            info.append((v, qv, kw, vw))
+
+        chunk = max(1, max_chunk_elems // max(1, P * g))
+        for c0 in range(0, len(info), chunk):
+            part = info[c0: c0 + chunk]
+            for kv in range(Hkv):
+                hs = slice(kv * g, (kv + 1) * g)
+                Q = np.concatenate([qv[hs] for _, qv, _, _ in part], axis=0)   # [c*g][d]
+                S_pre = (Q @ Kp[kv].T) * scale if P > 0 else np.zeros((Q.shape[0], 0))
+                for n, (v, qv, kw, vw) in enumerate(part):
+                    s_pre = S_pre[n * g:(n + 1) * g]                        # [g][P]
+                    s_win = (qv[hs] @ kw[:, kv].T) * scale                  # [g][D+1]
+                    s = np.concatenate([s_pre, s_win], axis=1)              # the node's key list
+                    m = s.max(axis=1, keepdims=True)
+                    e = np.exp(s - m)
+                    Z = e.sum(axis=1)
+                    o = e[:, :P] @ Vp[kv] + e[:, P:] @ vw[:, kv]
+                    out[b * N + v, hs] = o / Z[:, None]
+                    lse2[b * N + v, hs] = (m[:, 0] + np.log(Z)) / LN2
+    return out, lse2

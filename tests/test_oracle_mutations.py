@@ -1,0 +1,173 @@
+"""Planted mistakes in the oracle (on the CPU) must be caught by its pins.
+
+Each case swaps one oracle function for a plausibly wrong version (a wrong
+sign, a dropped term, an off-by-one, a transposed operand, the wrong tie rule)
+and runs the pin that should catch it; the pin must then fail.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle.attention as A
+import oracle.compact as C
+import oracle.merge as M
+import oracle.rope as R
+import oracle.tree as T
+import oracle.walk as W
+from tests import test_oracle_attention as PA
+from tests import test_oracle_tree as PT
+from tests import test_oracle_walk_compact as PW
+from tests.conftest import load_golden
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except (AssertionError, ValueError, IndexError):
+        return True
+    return False
+
+
+def _rope_wrong_sign(x, pos, theta):
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * R.inv_freq(d, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
+
+
+def _rope_adjacent_pairs(x, pos, theta):
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * R.inv_freq(d, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x1 * c - x2 * s
+    out[..., 1::2] = x2 * c + x1 * s
+    return out
+
+
+def test_rope_mutations_caught(monkeypatch):
+    for bad in (_rope_wrong_sign, _rope_adjacent_pairs):
+        monkeypatch.setattr(R, "rotate", bad)
+        assert _fails(PA.test_rope_matches_complex_rotation)
+        assert _fails(PA.test_chain_equals_causal_attention)
+
+
+def test_attention_mutations_caught(monkeypatch):
+    orig = A.verify_attention
+
+    def no_scale(*a, **k):
+        k["scale"] = 1.0
+        return orig(*a, **k)
+    monkeypatch.setattr(A, "verify_attention", no_scale)
+    assert _fails(PA.test_chain_equals_causal_attention)
+    monkeypatch.setattr(A, "verify_attention", orig)
+
+    # query rotated at the node's index instead of its depth
+    orig_root_path = A.root_path
+
+    def q_at_index(parents, v):
+        return list(range(v + 1)) if v < len(parents) else orig_root_path(parents, v)
+    monkeypatch.setattr(A, "root_path", q_at_index)
+    assert _fails(PA.test_each_node_is_its_own_root_path, [-1, 0, 0, 1, 2])
+    monkeypatch.setattr(A, "root_path", orig_root_path)
+
+    # wrong GQA mapping: head h reads KV head h % Hkv
+    def mod_heads(q, k_new, v_new, k_cache, v_cache, *rest, **kw):
+        g = q.shape[1] // rest[3]
+        perm = np.arange(q.shape[1]).reshape(g, -1).T.reshape(-1)
+        o, l = orig(q[:, perm], k_new, v_new, k_cache, v_cache, *rest, **kw)
+        inv = np.argsort(perm)
+        return o[:, inv], l[:, inv]
+    monkeypatch.setattr(A, "verify_attention", mod_heads)
+    assert _fails(PA.test_gqa_head_mapping_and_scale)
+
+
+def test_tree_mutations_caught(monkeypatch):
+    orig = T.ancestors
+    monkeypatch.setattr(T, "ancestors", lambda p, i: orig(p, i)[1:] or [i])   # drops self
+    assert _fails(PT.test_visibility_matrix_matches_page, load_golden)
+    monkeypatch.setattr(T, "ancestors", orig)
+
+    orig_links = T.links
+
+    def links_descending(parents):
+        n = len(parents)
+        nt = np.full(n, -1, np.int32)
+        ns = np.full(n, -1, np.int32)
+        for p in range(n):
+            kids = [j for j in range(n) if int(parents[j]) == p][::-1]
+            if kids:
+                nt[p] = kids[0]
+            for a, b in zip(kids, kids[1:]):
+                ns[a] = b
+        return nt, ns
+    monkeypatch.setattr(T, "links", links_descending)
+    assert _fails(PT.test_links_examples, load_golden, "ddtree_retrieve.txt")
+    monkeypatch.setattr(T, "links", orig_links)
+
+    monkeypatch.setattr(T, "positions", lambda vc, depth: np.arange(len(depth)) + int(vc))
+    assert _fails(PT.test_positions_examples, load_golden)
+
+
+def test_walk_mutations_caught(monkeypatch):
+    def last_match(parents, draft, argmax):
+        parents = [int(x) for x in parents]
+        n = len(parents)
+        path, cur = [0], 0
+        while True:
+            m = [j for j in range(n) if parents[j] == cur and int(draft[j]) == int(argmax[cur])]
+            if not m:
+                break
+            path.append(m[-1])
+            cur = m[-1]
+        ap = np.full(n, -1, np.int32)
+        at = np.full(n, -1, np.int32)
+        ap[: len(path)] = path
+        at[: len(path)] = [int(argmax[u]) for u in path]
+        return len(path), ap, at
+    monkeypatch.setattr(W, "greedy_walk", last_match)
+    assert _fails(PW.test_walk_with_duplicates_follows_the_definition, 4)
+
+    def child_token_compared(parents, draft, argmax):   # compares argmax at the child
+        parents = [int(x) for x in parents]
+        n = len(parents)
+        path, cur = [0], 0
+        while True:
+            m = [j for j in range(n) if parents[j] == cur and int(draft[j]) == int(argmax[j])]
+            if not m:
+                break
+            path.append(m[0])
+            cur = m[0]
+        ap = np.full(n, -1, np.int32)
+        at = np.full(n, -1, np.int32)
+        ap[: len(path)] = path
+        at[: len(path)] = [int(argmax[u]) for u in path]
+        return len(path), ap, at
+    monkeypatch.setattr(W, "greedy_walk", child_token_compared)
+    assert _fails(PW.test_walk_examples, load_golden, "accept_0_2_5_6.txt")
+
+
+def test_compact_and_merge_mutations_caught(monkeypatch):
+    def in_place_descending(buffers, wl, path, alen):
+        path = np.asarray(path)
+        B, N = path.shape
+        out = []
+        for buf in buffers:
+            new = np.array(buf, copy=True)
+            for b in range(B):
+                for t in reversed(range(int(alen[b]))):
+                    new[wl[b * N + t]] = new[wl[b * N + int(path[b, t])]]
+            out.append(new)
+        return out
+    monkeypatch.setattr(C, "compact_window_rows", in_place_descending)
+    assert _fails(PW.test_compact_overlap_reads_before_writes)
+
+    monkeypatch.setattr(M, "merge_states",
+                        lambda outs, ls: (np.mean(np.asarray(outs, float), axis=0), np.max(ls, axis=0)))
+    assert _fails(PA.test_merge_scalar_example, load_golden)
+    assert math.isfinite(1.0)
