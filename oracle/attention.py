@@ -26,6 +26,16 @@ positions array or the cache's window slots.
 Readings taken where the pages are silent: scale 1/sqrt(d); query head h reads
 KV head h // (Hq/Hkv); RoPE is the rotate-half form (oracle.rope).
 
+Precision of the rotated tensors: the paged K/V cache is bf16, and a window
+node's key enters attention as its slot holds it ([TS] "Position follows
+depth, slot follows node index": node i's rotated K is written to its slot),
+i.e. RoPE(k_new) rounded to bf16. The query reaches attention in the model
+dtype ([TS] "One tree attention", FP8 paragraph: the window kernel takes the
+unquantized query), i.e. RoPE(q) rounded to bf16. ``rope_out="bf16"`` (the
+default) applies both roundings (round to nearest, ties to even, from the
+exact fp64 rotation); ``rope_out=None`` keeps the exact rotation. Everything
+after that is fp64.
+
 The prefix scores of many nodes are formed with one matrix product per KV
 head (the same dot products, batched); each node's softmax is then taken over
 its own concatenated key list.
@@ -51,6 +61,14 @@ def widen(a) -> np.ndarray:
     return a.astype(np.float64)
 
 
+def round_bf16(x) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value (8 significant bits, ties
+    to even), returned as fp64. Finite normal-range inputs only (as here)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                      # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
 def prefix_slots(page_table_row, P: int, page_size: int) -> np.ndarray:
     pos = np.arange(P, dtype=np.int64)
     return np.asarray(page_table_row, dtype=np.int64)[pos // page_size] * page_size + pos % page_size
@@ -59,15 +77,17 @@ def prefix_slots(page_table_row, P: int, page_size: int) -> np.ndarray:
 def verify_attention(q, k_new, v_new, k_cache, v_cache, page_table, prefix_len, parents,
                      Hkv: int, theta: float, page_size: int = 64, scale: Optional[float] = None,
                      rows: Optional[Iterable] = None, q_rotated: bool = False,
-                     max_chunk_elems: int = 1 << 24):
+                     rope_out: Optional[str] = "bf16", max_chunk_elems: int = 1 << 24):
     """Returns (out [B*N][Hq][d] fp64, lse2 [B*N][Hq] fp64).
 
     q: [B*N][Hq][d]; k_new, v_new: [B*N][Hkv][d]; k_cache, v_cache:
     [slots][Hkv][d] (bf16 bits or floats); page_table int [B][max_pages];
     prefix_len int [B]; parents int [B][N]. ``rows`` restricts the work to the
     given (b, v) pairs; the other rows are NaN. ``q_rotated`` skips the query
-    rotation (the caller passes already-rotated queries).
+    rotation (the caller passes already-rotated queries). ``rope_out`` is the
+    storage precision of the rotated query and window keys ("bf16" or None).
     """
+    rnd = round_bf16 if rope_out == "bf16" else (lambda a: a)
     parents = np.asarray(parents)
     B, N = parents.shape
     q = np.asarray(q)
@@ -96,11 +116,11 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, page_table, prefix_len, 
             path = root_path(parents[b], v)
             D = len(path) - 1
             rows_bn = [b * N + u for u in path]
-            kw = rope.rotate(widen(np.asarray(k_new)[rows_bn]), P + np.arange(D + 1)[:, None], theta)
+            kw = rnd(rope.rotate(widen(np.asarray(k_new)[rows_bn]), P + np.arange(D + 1)[:, None], theta))
             vw = widen(np.asarray(v_new)[rows_bn])                      # [D+1][Hkv][d]
             qv = widen(q[b * N + v])
             if not q_rotated:
-                qv = rope.rotate(qv, P + D, theta)                      # [Hq][d]
+                qv = rnd(rope.rotate(qv, P + D, theta))                 # [Hq][d]
             info.append((v, qv, kw, vw))
 
         chunk = max(1, max_chunk_elems // max(1, P * g))

@@ -20,6 +20,13 @@ from oracle import tree as T
 THETA = 5.0e5
 
 
+def _va(*a, **k):
+    """The oracle with the exact rotation (these pins use non-bf16 inputs);
+    the bf16 rounding of rotated tensors is pinned on its own below."""
+    k.setdefault("rope_out", None)
+    return A.verify_attention(*a, **k)
+
+
 # ----------------------------------------------------------------------------
 # an independent causal attention over one sequence
 # ----------------------------------------------------------------------------
@@ -101,7 +108,7 @@ def test_chain_equals_causal_attention():
     B, N, Hq, Hkv, d, P, page = 2, 6, 4, 2, 16, 9, 4
     parents = list(range(-1, N - 1))
     q, kn, vn, kc, vc, table, plen, par = _case(rng, B, N, Hq, Hkv, d, P, parents, page)
-    out, lse2 = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out, lse2 = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     for b in range(B):
         kp, vp = _prefix_seq(kc, vc, table, b, P, page)
         qseq = np.concatenate([np.zeros((P, Hq, d)), q[b * N:(b + 1) * N]])
@@ -124,7 +131,7 @@ def test_each_node_is_its_own_root_path(parents):
     N = len(parents)
     B, Hq, Hkv, d, P, page = 1, 4, 2, 8, 5, 4
     q, kn, vn, kc, vc, table, plen, par = _case(rng, B, N, Hq, Hkv, d, P, parents, page)
-    out, lse2 = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out, lse2 = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     kp, vp = _prefix_seq(kc, vc, table, 0, P, page)
     for v in range(N):
         path = T.root_path(parents, v)
@@ -141,12 +148,12 @@ def test_star_sees_prefix_root_and_itself():
     N, Hq, Hkv, d, P, page = 5, 2, 1, 8, 7, 4
     parents = [-1, 0, 0, 0, 0]
     q, kn, vn, kc, vc, table, plen, par = _case(rng, 1, N, Hq, Hkv, d, P, parents, page)
-    out, _ = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out, _ = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     # changing node 3's K/V changes only row 3
     kn2, vn2 = kn.copy(), vn.copy()
     kn2[3] += 1.0
     vn2[3] -= 2.0
-    out2, _ = A.verify_attention(q, kn2, vn2, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out2, _ = _va(q, kn2, vn2, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     changed = [v for v in range(N) if not np.array_equal(out[v], out2[v])]
     assert changed == [3]
 
@@ -157,7 +164,7 @@ def test_non_ancestors_are_never_read():
     parents = [-1, 0, 0, 1, 2, 1, 0]
     N, Hq, Hkv, d, P, page = len(parents), 4, 2, 8, 6, 4
     q, kn, vn, kc, vc, table, plen, par = _case(rng, 1, N, Hq, Hkv, d, P, parents, page)
-    out, lse2 = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out, lse2 = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     for v in range(N):
         anc = set(T.ancestors(parents, v))
         kn2, vn2 = kn.copy(), vn.copy()
@@ -165,7 +172,7 @@ def test_non_ancestors_are_never_read():
             if j not in anc:
                 kn2[j] = np.nan
                 vn2[j] = np.inf
-        o2, l2 = A.verify_attention(q, kn2, vn2, kc, vc, table, plen, par, Hkv, THETA,
+        o2, l2 = _va(q, kn2, vn2, kc, vc, table, plen, par, Hkv, THETA,
                                     page_size=page, rows=[(0, v)])
         assert np.array_equal(o2[v], out[v]) and np.array_equal(l2[v], lse2[v])
 
@@ -179,10 +186,10 @@ def test_gqa_head_mapping_and_scale():
     q, kn, vn, kc, vc, table, plen, par = _case(rng, 1, N, Hq, Hkv, d, P, parents, page)
     q[:, 1] = q[:, 0]
     q[:, 3] = q[:, 2]
-    out, lse2 = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out, lse2 = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     assert np.array_equal(out[:, 0], out[:, 1]) and np.array_equal(out[:, 2], out[:, 3])
     assert not np.allclose(out[:, 0], out[:, 2])
-    out2, _ = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA,
+    out2, _ = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA,
                                  page_size=page, scale=1.0 / math.sqrt(d))
     assert np.array_equal(out, out2)
 
@@ -192,7 +199,7 @@ def test_zero_prefix_root_row_is_its_own_value():
     rng = np.random.default_rng(8)
     N, Hq, Hkv, d, page = 3, 2, 1, 8, 4
     q, kn, vn, kc, vc, table, plen, par = _case(rng, 1, N, Hq, Hkv, d, 0, [-1, 0, 0], page)
-    out, lse2 = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out, lse2 = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     for h in range(Hq):
         assert np.allclose(out[0, h], vn[0, 0])
         s = np.dot(q[0, h], kn[0, 0]) / math.sqrt(d)     # both at position 0: no rotation
@@ -204,10 +211,10 @@ def test_softmax_shift_invariance_and_bf16_widening():
     parents = [-1, 0, 1, 0]
     N, Hq, Hkv, d, P, page = 4, 2, 1, 8, 5, 4
     q, kn, vn, kc, vc, table, plen, par = _case(rng, 1, N, Hq, Hkv, d, P, parents, page)
-    out, lse2 = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    out, lse2 = _va(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
     # values shifted by a constant vector: outputs shift by the same vector
     c = rng.standard_normal(d)
-    out2, lse2b = A.verify_attention(q, kn, vn + c, kc, vc + c, table, plen, par, Hkv, THETA,
+    out2, lse2b = _va(q, kn, vn + c, kc, vc + c, table, plen, par, Hkv, THETA,
                                      page_size=page)
     assert np.allclose(out2, out + c, atol=1e-12) and np.allclose(lse2b, lse2)
     bits = np.array([0x3F80, 0xC000, 0x0001], np.uint16)        # 1.0, -2.0, smallest subnormal
@@ -237,3 +244,51 @@ def test_merge_equals_softmax_over_union():
     full = logsumexp(s)
     assert np.allclose(o, np.exp(s - full) @ v, atol=1e-13)
     assert np.isclose(l2, full / math.log(2))
+
+
+def test_round_bf16_against_torch_cast_and_ties():
+    """round_bf16 is round-to-nearest-even to 8 significant bits: it agrees with
+    torch's float32 -> bfloat16 cast on float32 inputs, keeps bf16 values, and
+    sends exact midpoints to the even neighbour."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(20)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(A.round_bf16(x.astype(np.float64)), want)
+    assert A.round_bf16(np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -3.0])).tolist() == \
+        [1.0, 1.0, 1.0 + 2.0 ** -6, -3.0]
+
+
+def test_bf16_storage_of_rotated_tensors():
+    """With rope_out='bf16' the oracle equals the exact-rotation oracle fed
+    with rotated-then-rounded tensors (window keys rounded at their positions,
+    queries at theirs): the chain case against the causal reference."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    B, N, Hq, Hkv, d, P, page = 1, 5, 4, 2, 16, 7, 4
+    parents = list(range(-1, N - 1))
+    q, kn, vn, kc, vc, table, plen, par = _case(rng, B, N, Hq, Hkv, d, P, parents, page)
+    out, lse2 = A.verify_attention(q, kn, vn, kc, vc, table, plen, par, Hkv, THETA, page_size=page)
+    pos = P + np.arange(N)
+
+    def rounded(x, p):
+        r = rope_complex(x, p[:, None], THETA).astype(np.float32)
+        return torch.from_numpy(r).to(torch.bfloat16).to(torch.float64).numpy()
+    q_r, k_r = rounded(q, pos), rounded(kn, pos)
+    kp, vp = _prefix_seq(kc, vc, table, 0, P, page)
+    kseq = np.concatenate([kp, k_r])
+    vseq = np.concatenate([vp, vn])
+    # causal attention with already-rotated keys and queries (n_pre_rotated = everything)
+    L = P + N
+    outs, lses = [], []
+    for t in range(P, L):
+        o_t, l_t = [], []
+        for h in range(Hq):
+            s = kseq[: t + 1, h // (Hq // Hkv)] @ q_r[t - P, h] / math.sqrt(d)
+            l = logsumexp(s)
+            o_t.append(np.exp(s - l) @ vseq[: t + 1, h // (Hq // Hkv)])
+            l_t.append(l / math.log(2))
+        outs.append(o_t)
+        lses.append(l_t)
+    # the exact-rotation outputs differ by the rounding; the bf16 ones match
+    assert np.allclose(out, np.array(outs), atol=1e-6) and np.allclose(lse2, np.array(lses), atol=1e-6)
