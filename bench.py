@@ -1,0 +1,401 @@
+"""Benchmark of one full target-verify step of draft-tree speculative decoding.
+
+A step is one pass of the whole hot path over one synthetic batch:
+build_tree_mask -> write_window_kv -> tree_verify_attention (prefix pass +
+window/merge pass) -> verify_tree_greedy -> compact_window_rows ->
+compact_rows. Inputs are resident in HBM when the timed region starts; L2 is
+flushed (512 MiB write) before every timed step, outside the step's events.
+
+Default workload: eagle2_p8192_n64 (B=32, Hq=32, Hkv=8, d=128, P=8192, N=64),
+the long-prefix regime (P >= 8192) where the attention must reach its
+roofline. ``--workload`` picks another.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path shards by request with no exchange); value = all ranks' rows / the
+slowest rank's time. ``--impl reference`` times the CPU oracle (fp64 NumPy) on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from draft_tree_speculative_gb300 import synth  # noqa: E402
+
+METRIC = "tree-verify attention rows/s & % of HBM/tensor roofline; verify_tree µs/step"
+ATTN_SOURCES = ("draft_tree_speculative_gb300/csrc/attention.cu", "draft_tree_speculative_gb300/csrc/tcgen05.cuh",
+                "draft_tree_speculative_gb300/csrc/common.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="eagle2_p8192_n64", choices=list(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes / FLOPs of one tree_verify_attention call
+# ----------------------------------------------------------------------------
+
+def attention_work(inp: synth.VerifyInputs):
+    w = inp.w
+    P = inp.vc.astype(np.int64)
+    kv_row = w.Hkv * w.d * 2                      # one slot of K (or V), bf16
+    kv = 2 * kv_row * (int(P.sum()) + w.B * w.N)  # prefix + window K and V, read once per KV head
+    rows = w.B * w.N * w.Hq
+    q = out = rows * w.d * 2
+    small = rows * 4 + w.B * w.N * (8 + 4) + inp.layout.page_table.size * 4 + w.B * 4
+    bytes_ = kv + q + out + small
+    depth_sum = int(inp.depth.sum()) + w.B * w.N
+    flops = 4 * w.N * w.Hq * w.d * int(P.sum()) + 4 * w.Hq * w.d * depth_sum
+    return bytes_, flops
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def attention_source_hash():
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per attention call from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != attention_source_hash():
+        return None
+    return e.get("bytes_per_call")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ----------------------------------------------------------------------------
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+def oracle_sample(inp: synth.VerifyInputs, b: int, nodes):
+    """Oracle work for `nodes` of request b: attention rows, the walk and the
+    compaction of that request. Returns the number of verify rows done."""
+    from oracle import attention as OA
+    from oracle import compact as OC
+    from oracle import walk as OW
+    w = inp.w
+    OA.verify_attention(inp.q, inp.k_new, inp.v_new, inp.k_cache, inp.v_cache, inp.layout.page_table, inp.vc,
+                        inp.parents, w.Hkv, w.rope_theta, page_size=w.page_size, rows=[(b, v) for v in nodes])
+    alen, path, _ = OW.greedy_walk(inp.parents[b], inp.draft[b], inp.target_argmax[b])
+    wl = inp.layout.write_locations[b * w.N:(b + 1) * w.N]
+    rows = np.arange(w.N)
+    kv = [inp.k_cache[wl], inp.v_cache[wl]]
+    OC.compact_window_rows(kv, rows, path[None], [alen])
+    if inp.hidden is not None:
+        OC.compact_hidden_rows(inp.hidden[b * w.N:(b + 1) * w.N], path[None], [alen])
+    return len(nodes)
+
+
+def cpu_rows_per_s(inp, steps=1, nodes_per_step=8):
+    w = inp.w
+    n_nodes = min(nodes_per_step, w.N)
+    rows = 0
+    t0 = time.perf_counter()
+    for s in range(steps):
+        b = s % w.B
+        nodes = [(s * n_nodes + k) % w.N for k in range(n_nodes)]
+        rows += oracle_sample(inp, b, nodes)
+    dt = time.perf_counter() - t0
+    return rows / dt, dt, f"{n_nodes} verify rows (all heads) of one request per step, plus that request's walk " \
+                          f"and compaction; {steps} step(s)"
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from draft_tree_speculative_gb300 import lib
+    from draft_tree_speculative_gb300.step import DeviceBatch, run_step
+
+    lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w)
+    db = DeviceBatch(inp, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    names = ("mask", "window_kv", "attention", "walk", "compact")
+    calls = (db.mask_step, db.window_kv_step, db.attention_step, db.walk_step, db.compact_step)
+    launches_per_step = 7 if db.max_prefix > 0 else 6
+
+    def one_step(ev=None):
+        for k, c in enumerate(calls):
+            if ev is not None:
+                ev[k].record(stream)
+            c(stream)
+        if ev is not None:
+            ev[len(calls)].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            one_step()
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0, "device reported an error during warm-up"
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for s in range(args.steps):
+                flush.fill_(1)
+                one_step(events[s])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    per_call = {n: [] for n in names}
+    step_ms = []
+    for ev in events:
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+        for k, n in enumerate(names):
+            per_call[n].append(ev[k].elapsed_time(ev[k + 1]))
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    rows_per_step = w.B * w.N
+    value = world * rows_per_step / (ms_per_step / 1e3)
+
+    # roofline of the attention call (prefix pass + window/merge pass)
+    attn_ms = statistics.mean(per_call["attention"])
+    bytes_, flops = attention_work(inp)
+    hbm, tf_burst, tf_sus, src = load_peaks()
+    t_hbm = bytes_ / (hbm * 1e9)
+    t_mma = flops / (tf_sus * 1e12)
+    if t_hbm >= t_mma:
+        roof = {"bound": "hbm", "achieved": bytes_ / (attn_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (attn_ms / 1e3) / 1e12, "peak": tf_sus, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(args.workload)
+    roof["kernel"] = "tree_verify_attention (tree_prefix_kernel + tree_window_kernel)"
+    roof["algorithmic_bytes"] = bytes_
+    roof["algorithmic_flops"] = flops
+    roof["peak_source"] = f"{src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})"
+    roof["roofline_us"] = max(t_hbm, t_mma) * 1e6
+    roof["attention_us"] = attn_ms * 1e3
+
+    # end to end through the public API: pinned host inputs in, result out
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(db, k).cpu().pin_memory() for k in
+                ("q", "k_new", "v_new", "parents", "depth", "vc", "draft", "target_argmax")}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        out_alen = torch.empty_like(db.accept_len, device="cpu").pin_memory()
+        out_tok = torch.empty_like(db.accepted_tokens, device="cpu").pin_memory()
+        d2h = out_alen.numel() * 4 + out_tok.numel() * 4
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for s in range(args.warmup + args.steps):
+                flush.fill_(1)
+                if s >= args.warmup:
+                    ev[s - args.warmup][0].record(stream)
+                for k, t in host.items():
+                    getattr(db, k).copy_(t, non_blocking=True)
+                run_step(db, stream)
+                out_alen.copy_(db.accept_len, non_blocking=True)
+                out_tok.copy_(db.accepted_tokens, non_blocking=True)
+                if s >= args.warmup:
+                    ev[s - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = sum(a.elapsed_time(b) for a, b in ev)
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * rows_per_step / (e_ms / args.steps / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    assert int(db.err.item()) == 0, "device reported an error"
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the workload)",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "prefix_len": int(inp.vc.max()), "page_size": w.page_size, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed step (512 MiB write, outside the step's events)"},
+        "roofline": roof,
+        "verify_tree_us": statistics.median(per_call["walk"]) * 1e3,
+        "kernels_us": {n: statistics.median(v) * 1e3 for n, v in per_call.items()},
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region": wall,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    clocks = clk.summary()
+    if clocks is not None:
+        line["clocks"] = clocks
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, sample = cpu_rows_per_s(inp, steps=1, nodes_per_step=min(16, w.N))
+        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    return line
+
+
+def run_reference(args):
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w)
+    cpu_rows_per_s(inp, steps=args.warmup, nodes_per_step=2)
+    v, dt, sample = cpu_rows_per_s(inp, steps=args.steps, nodes_per_step=2)
+    line = {
+        "metric": METRIC, "value": v, "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes of the workload)",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "prefix_len": int(inp.vc.max()), "page_size": w.page_size, "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

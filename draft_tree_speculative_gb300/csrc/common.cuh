@@ -1,0 +1,75 @@
+// Shared device helpers of the CUDA path: error reporting, bf16 packing and
+// RoPE angles. Nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dts.h"
+
+namespace dts {
+
+constexpr int kMaxNodes = 64;
+
+// First error wins: a zero word becomes `code`; later errors leave it alone.
+__device__ __forceinline__ void report(int32_t *err, int code) {
+  if (err != nullptr) atomicCAS(reinterpret_cast<int *>(err), 0, code);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Pack two floats as bf16 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// RoPE angles.
+//
+// Position p (an integer < 2^24) and frequency w_k = theta^(-2k/d) give the
+// angle p * w_k, which reaches ~1.3e5 rad at the long-context positions. A
+// plain fp32 product would carry ~1e-2 rad of error there. The host passes
+// w_k as an unevaluated sum hi + lo of two floats (from a double); the device
+// forms p * w exactly as a float-float pair (Dekker's product by FMA: the
+// rounding error of p*hi is fma(p, hi, -p*hi)), then reduces modulo 2*pi
+// with a three-part constant (Cody and Waite's additive range reduction).
+// The first FMA of the reduction is exact because both terms are multiples of
+// ulp(2*pi) and the result is below 2^24 of those units. The reduced angle is
+// in [-pi, pi] up to ~3e-7 rad, where the hardware sine/cosine are accurate
+// to ~5e-7; both are far below bf16 resolution.
+// ---------------------------------------------------------------------------
+struct RopeFreqs {
+  float2 w[64];  // (hi, lo) for k < d/2, d <= 128
+};
+
+__device__ __forceinline__ float rope_reduced_angle(int pos, float2 w) {
+  const float p = static_cast<float>(pos);
+  const float a_hi = __fmul_rn(p, w.x);  // rounded product, never contracted
+  const float a_err = fmaf(p, w.x, -a_hi);
+  const float a_lo = fmaf(p, w.y, a_err);
+  const float kTwoPi1 = 6.28318548202514648438f;        // float(2*pi)
+  const float kTwoPi2 = -1.74845553146951715462e-07f;   // float(2*pi - kTwoPi1)
+  const float kTwoPi3 = -6.86049804002352749122e-15f;   // float(2*pi - kTwoPi1 - kTwoPi2)
+  const float kInvTwoPi = 0.15915493667125701904f;
+  const float n = rintf(a_hi * kInvTwoPi);
+  float r = fmaf(-n, kTwoPi1, a_hi);
+  r = fmaf(-n, kTwoPi2, r);
+  r = fmaf(-n, kTwoPi3, r);
+  return r + a_lo;
+}
+
+__device__ __forceinline__ void rope_sincos(int pos, float2 w, float *s, float *c) {
+  __sincosf(rope_reduced_angle(pos, w), s, c);
+}
+
+}  // namespace dts
+
+// Host helpers (defined in api.cu).
+namespace dts_host {
+void make_rope_freqs(float theta, int d, dts::RopeFreqs *out);
+int launch_status();  // DTS_OK or DTS_ERR_CUDA from cudaGetLastError()
+int sm_count();
+}  // namespace dts_host

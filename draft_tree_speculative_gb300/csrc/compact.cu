@@ -1,0 +1,205 @@
+// Compaction of the accepted path: KV rows of every buffer in a cache group's
+// address table, and hidden rows plus positions.
+//
+// [TS] "The tree is a parameter of the chain path": the path's KV of every
+// layer moves to the window's leading slots by a word copy that does not care
+// about dtype, and the hidden rows move to the front of the window with the
+// positions back to vc + i. [MI] "Discarding the rejected branches' KV":
+// destinations are the first accept_len window slots.
+//
+// Snapshot order: the accepted path is strictly increasing with path[0] = 0,
+// so path[t] >= t. A row written for step t (window slot t) is never the
+// source of a later step t2 > t (whose source is slot path[t2] >= t2 > t).
+// The copy therefore runs in rounds over the moved rows in ascending order:
+// each round loads all of its words into registers, the block synchronises,
+// then stores them. Within a round every load precedes every store; across
+// rounds the argument above holds.
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kPerThread = 8;  // words staged per thread per round
+
+// Validate one request's packed path. Fills dst/src with the moved rows (in
+// window-slot units) and returns their count, or -1 for a bad path.
+__device__ int collect_moves(const int32_t *__restrict__ path, int alen, int N, int *dst, int *src) {
+  if (alen < 1 || alen > N || path[0] != 0) return -1;
+  int n = 0;
+  for (int t = 1; t < alen; ++t) {
+    const int p = path[t];
+    if (p <= path[t - 1] || p >= N) return -1;
+    if (p != t) {
+      dst[n] = t;
+      src[n] = p;
+      ++n;
+    }
+  }
+  return n;
+}
+
+template <typename Word>
+__device__ void move_rows(char *base, int64_t stride, int row_words, const int64_t *dst_slot,
+                          const int64_t *src_slot, int n_moved) {
+  const int64_t total = static_cast<int64_t>(n_moved) * row_words;
+  for (int64_t r0 = 0; r0 < total; r0 += static_cast<int64_t>(kThreads) * kPerThread) {
+    Word v[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int64_t e = r0 + static_cast<int64_t>(k) * kThreads + threadIdx.x;
+      if (e < total) {
+        const int m = static_cast<int>(e / row_words);
+        const int c = static_cast<int>(e % row_words);
+        v[k] = reinterpret_cast<const Word *>(base + src_slot[m] * stride)[c];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int64_t e = r0 + static_cast<int64_t>(k) * kThreads + threadIdx.x;
+      if (e < total) {
+        const int m = static_cast<int>(e / row_words);
+        const int c = static_cast<int>(e % row_words);
+        reinterpret_cast<Word *>(base + dst_slot[m] * stride)[c] = v[k];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__device__ void move_rows_any(char *base, int64_t stride, int row_bytes, const int64_t *dst_slot,
+                              const int64_t *src_slot, int n_moved) {
+  const uint64_t a = reinterpret_cast<uint64_t>(base) | static_cast<uint64_t>(stride) |
+                     static_cast<uint64_t>(row_bytes);
+  if ((a & 15) == 0) move_rows<uint4>(base, stride, row_bytes / 16, dst_slot, src_slot, n_moved);
+  else if ((a & 7) == 0) move_rows<uint2>(base, stride, row_bytes / 8, dst_slot, src_slot, n_moved);
+  else move_rows<uint32_t>(base, stride, row_bytes / 4, dst_slot, src_slot, n_moved);
+}
+
+// grid (n_buffers, B)
+__global__ void __launch_bounds__(kThreads) compact_window_rows_kernel(
+    const dts_kv_buffer *__restrict__ table, int n_buffers, const int64_t *__restrict__ wl,
+    const int32_t *__restrict__ accepted_path, const int32_t *__restrict__ accept_len, int N,
+    int32_t *err) {
+  __shared__ int s_dst[dts::kMaxNodes], s_src[dts::kMaxNodes];
+  __shared__ int64_t s_dslot[dts::kMaxNodes], s_sslot[dts::kMaxNodes];
+  __shared__ int s_n, s_skip;
+  const int l = blockIdx.x;
+  const int b = blockIdx.y;
+  const dts_kv_buffer e = table[l];
+  if (threadIdx.x == 0) {
+    s_skip = 0;
+    const uint64_t a = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
+                       static_cast<uint64_t>(e.row_bytes);
+    if (e.base == nullptr || (a & 3) != 0 || e.row_bytes <= 0 || e.slot_stride_bytes < e.row_bytes ||
+        e.num_slots <= 0 || e.reserved != 0) {
+      dts::report(err, DTS_DEV_BAD_BUFFER);
+      s_skip = 1;
+    }
+  }
+  __syncthreads();
+  if (s_skip) return;
+  // Each physical region moves once: skip this entry if another entry with the
+  // same stride covers its rows (equal ranges: the lower index moves).
+  const uint64_t lo = reinterpret_cast<uint64_t>(e.base);
+  const uint64_t hi = lo + static_cast<uint64_t>(e.row_bytes);
+  for (int o = threadIdx.x; o < n_buffers; o += kThreads) {
+    if (o == l) continue;
+    const dts_kv_buffer f = table[o];
+    if (f.slot_stride_bytes != e.slot_stride_bytes || f.base == nullptr) continue;
+    const uint64_t flo = reinterpret_cast<uint64_t>(f.base);
+    const uint64_t fhi = flo + static_cast<uint64_t>(f.row_bytes);
+    if (fhi <= lo || hi <= flo) continue;                  // disjoint
+    const bool inside = flo <= lo && hi <= fhi;
+    const bool outside = lo <= flo && fhi <= hi;
+    if (inside && !(outside && o > l)) atomicOr(&s_skip, 1);  // covered by o
+    else if (!inside && !outside) atomicOr(&s_skip, 2);        // partial overlap
+  }
+  __syncthreads();
+  if (s_skip) {
+    if (threadIdx.x == 0 && (s_skip & 2) && b == 0) dts::report(err, DTS_DEV_BAD_BUFFER);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    const int n = collect_moves(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
+    if (n < 0) {
+      if (l == 0) dts::report(err, DTS_DEV_BAD_PATH);
+      s_n = 0;
+    } else {
+      int ok = n;
+      for (int m = 0; m < n; ++m) {
+        const int64_t d = wl[static_cast<int64_t>(b) * N + s_dst[m]];
+        const int64_t s = wl[static_cast<int64_t>(b) * N + s_src[m]];
+        if (d < 0 || d >= e.num_slots || s < 0 || s >= e.num_slots) {
+          dts::report(err, DTS_DEV_BAD_SLOT);
+          ok = 0;
+          break;
+        }
+        s_dslot[m] = d;
+        s_sslot[m] = s;
+      }
+      s_n = ok;
+    }
+  }
+  __syncthreads();
+  if (s_n == 0) return;
+  move_rows_any(static_cast<char *>(e.base), e.slot_stride_bytes, e.row_bytes, s_dslot, s_sslot, s_n);
+}
+
+// grid (B)
+__global__ void __launch_bounds__(kThreads) compact_rows_kernel(
+    char *__restrict__ hidden, int64_t row_bytes, int32_t *__restrict__ positions,
+    const int32_t *__restrict__ vc, const int32_t *__restrict__ accepted_path,
+    const int32_t *__restrict__ accept_len, int N, int32_t *err) {
+  __shared__ int s_dst[dts::kMaxNodes], s_src[dts::kMaxNodes];
+  __shared__ int64_t s_dslot[dts::kMaxNodes], s_sslot[dts::kMaxNodes];
+  __shared__ int s_n;
+  const int b = blockIdx.x;
+  if (positions != nullptr)
+    for (int i = threadIdx.x; i < N; i += kThreads) positions[static_cast<int64_t>(b) * N + i] = vc[b] + i;
+  if (hidden == nullptr) return;
+  if (threadIdx.x == 0) {
+    const int n = collect_moves(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
+    if (n < 0) dts::report(err, DTS_DEV_BAD_PATH);
+    for (int m = 0; m < n; ++m) {
+      s_dslot[m] = static_cast<int64_t>(b) * N + s_dst[m];
+      s_sslot[m] = static_cast<int64_t>(b) * N + s_src[m];
+    }
+    s_n = n < 0 ? 0 : n;
+  }
+  __syncthreads();
+  if (s_n == 0) return;
+  move_rows_any(hidden, row_bytes, static_cast<int>(row_bytes), s_dslot, s_sslot, s_n);
+}
+
+}  // namespace
+
+extern "C" int dts_compact_window_rows(const dts_kv_buffer *table, int n_buffers,
+                                       const int64_t *write_locations, const int32_t *accepted_path,
+                                       const int32_t *accept_len, int B, int N, int32_t *err_dev,
+                                       dts_stream_t stream) {
+  if (B < 0 || N < 1 || n_buffers < 0) return DTS_ERR_INVALID;
+  if (N > dts::kMaxNodes) return DTS_ERR_UNSUPPORTED;
+  if (B == 0 || n_buffers == 0) return DTS_OK;
+  if (n_buffers > 65535 || B > 65535) return DTS_ERR_UNSUPPORTED;
+  if (!table || !write_locations || !accepted_path || !accept_len) return DTS_ERR_INVALID;
+  compact_window_rows_kernel<<<dim3(n_buffers, B), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      table, n_buffers, write_locations, accepted_path, accept_len, N, err_dev);
+  return dts_host::launch_status();
+}
+
+extern "C" int dts_compact_rows(void *hidden, int64_t row_bytes, int32_t *positions, const int32_t *vc,
+                                const int32_t *accepted_path, const int32_t *accept_len, int B, int N,
+                                int32_t *err_dev, dts_stream_t stream) {
+  if (B < 0 || N < 1) return DTS_ERR_INVALID;
+  if (N > dts::kMaxNodes) return DTS_ERR_UNSUPPORTED;
+  if (B == 0 || (hidden == nullptr && positions == nullptr)) return DTS_OK;
+  if (hidden != nullptr && (row_bytes <= 0 || (row_bytes & 3) != 0 || row_bytes > (1ll << 30) ||
+                            (reinterpret_cast<uintptr_t>(hidden) & 3) != 0))
+    return DTS_ERR_INVALID;
+  if (hidden != nullptr && (!accepted_path || !accept_len)) return DTS_ERR_INVALID;
+  if (positions != nullptr && vc == nullptr) return DTS_ERR_INVALID;
+  compact_rows_kernel<<<B, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<char *>(hidden), row_bytes, positions, vc, accepted_path, accept_len, N, err_dev);
+  return dts_host::launch_status();
+}

@@ -1,0 +1,122 @@
+// Window K/V write: node i's key, rotated at positions[b][i] = vc + depth[i],
+// and its value go to the slot of logical position prefix_len[b] + i.
+// [TS] "Position follows depth, slot follows node index".
+//
+// One warp per (node, KV head). Lane l holds the rotate-half pairs
+// (2l, 2l+1 | d/2+2l, d/2+2l+1) for d = 128, or (l | d/2+l) for d = 64.
+#include "common.cuh"
+
+namespace {
+
+struct WindowKvArgs {
+  const uint16_t *k_new;
+  const uint16_t *v_new;
+  const int32_t *positions;
+  const int32_t *page_table;
+  const int32_t *prefix_len;
+  uint16_t *k_cache;
+  uint16_t *v_cache;
+  int64_t *write_locations;
+  int32_t *err;
+  int64_t num_slots;
+  int max_pages, page_shift, B, N, Hkv;
+  dts::RopeFreqs freqs;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) write_window_kv_kernel(const __grid_constant__ WindowKvArgs a) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = a.B * a.N * a.Hkv;
+  if (warp >= total) return;
+  const int h = warp % a.Hkv;
+  const int node = warp / a.Hkv;  // b * N + i
+  const int b = node / a.N;
+  const int i = node - b * a.N;
+  const int P = a.prefix_len[b];
+  const int ps = 1 << a.page_shift;
+  const int64_t logical = static_cast<int64_t>(P) + i;
+  const int64_t page = logical >> a.page_shift;
+  int64_t slot = -1;
+  if (P >= 0 && page < a.max_pages) {
+    const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + page];
+    const int64_t s = static_cast<int64_t>(pid) * ps + (logical & (ps - 1));
+    if (pid >= 0 && s < a.num_slots) slot = s;
+  }
+  if (slot < 0) {
+    if (lane == 0 && h == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
+    if (lane == 0 && h == 0 && a.write_locations) a.write_locations[node] = -1;
+    return;
+  }
+  if (lane == 0 && h == 0 && a.write_locations) a.write_locations[node] = slot;
+  const int pos = a.positions[node];
+  const uint16_t *kin = a.k_new + (static_cast<int64_t>(node) * a.Hkv + h) * D;
+  const uint16_t *vin = a.v_new + (static_cast<int64_t>(node) * a.Hkv + h) * D;
+  uint16_t *kout = a.k_cache + (slot * a.Hkv + h) * D;
+  uint16_t *vout = a.v_cache + (slot * a.Hkv + h) * D;
+  if constexpr (D == 128) {
+    const int k0 = 2 * lane;
+    const uint32_t x1 = reinterpret_cast<const uint32_t *>(kin)[lane];        // elems k0, k0+1
+    const uint32_t x2 = reinterpret_cast<const uint32_t *>(kin + 64)[lane];   // elems 64+k0, 64+k0+1
+    float s0, c0, s1, c1;
+    dts::rope_sincos(pos, a.freqs.w[k0], &s0, &c0);
+    dts::rope_sincos(pos, a.freqs.w[k0 + 1], &s1, &c1);
+    const float a0 = dts::bf16_lo(x1), a1 = dts::bf16_hi(x1);
+    const float b0 = dts::bf16_lo(x2), b1 = dts::bf16_hi(x2);
+    reinterpret_cast<uint32_t *>(kout)[lane] = dts::pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
+    reinterpret_cast<uint32_t *>(kout + 64)[lane] = dts::pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+    reinterpret_cast<uint2 *>(vout)[lane] = reinterpret_cast<const uint2 *>(vin)[lane];
+  } else {
+    const float a0 = __uint_as_float(static_cast<uint32_t>(kin[lane]) << 16);
+    const float b0 = __uint_as_float(static_cast<uint32_t>(kin[32 + lane]) << 16);
+    float s0, c0;
+    dts::rope_sincos(pos, a.freqs.w[lane], &s0, &c0);
+    const uint32_t r = dts::pack_bf16x2(a0 * c0 - b0 * s0, b0 * c0 + a0 * s0);
+    kout[lane] = static_cast<uint16_t>(r & 0xFFFFu);
+    kout[32 + lane] = static_cast<uint16_t>(r >> 16);
+    reinterpret_cast<uint32_t *>(vout)[lane] = reinterpret_cast<const uint32_t *>(vin)[lane];
+  }
+}
+
+}  // namespace
+
+extern "C" int dts_write_window_kv(const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
+                                   const int32_t *page_table, int max_pages, int page_size,
+                                   const int32_t *prefix_len, int B, int N, int Hkv, int d,
+                                   int64_t num_slots, float rope_theta, uint16_t *k_cache,
+                                   uint16_t *v_cache, int64_t *write_locations, int32_t *err_dev,
+                                   dts_stream_t stream) {
+  if (B < 0 || N < 1 || Hkv < 1 || max_pages < 1 || num_slots < 1) return DTS_ERR_INVALID;
+  if (N > dts::kMaxNodes || (d != 64 && d != 128)) return DTS_ERR_UNSUPPORTED;
+  if (page_size < 8 || page_size > 4096 || (page_size & (page_size - 1)) != 0) return DTS_ERR_UNSUPPORTED;
+  if (!(rope_theta > 0.f)) return DTS_ERR_INVALID;
+  if (B == 0) return DTS_OK;
+  if (!k_new || !v_new || !positions || !page_table || !prefix_len || !k_cache || !v_cache)
+    return DTS_ERR_INVALID;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+                       reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
+  if (al & 7) return DTS_ERR_INVALID;
+  WindowKvArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.positions = positions;
+  a.page_table = page_table;
+  a.prefix_len = prefix_len;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.write_locations = write_locations;
+  a.err = err_dev;
+  a.num_slots = num_slots;
+  a.max_pages = max_pages;
+  a.page_shift = __builtin_ctz(static_cast<unsigned>(page_size));
+  a.B = B;
+  a.N = N;
+  a.Hkv = Hkv;
+  dts_host::make_rope_freqs(rope_theta, d, &a.freqs);
+  const int64_t warps = static_cast<int64_t>(B) * N * Hkv;
+  const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 128) write_window_kv_kernel<128><<<blocks, 256, 0, s>>>(a);
+  else write_window_kv_kernel<64><<<blocks, 256, 0, s>>>(a);
+  return dts_host::launch_status();
+}

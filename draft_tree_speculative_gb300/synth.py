@@ -58,6 +58,7 @@ class Workload:
     hidden_dim: int = 4096
     fp8_layers: int = 0               # layers of fp8 K/V for compaction (K and V each)
     rope_theta: float = ROPE_THETA
+    page_size: int = PAGE_SIZE
 
     @property
     def group(self) -> int:
@@ -100,15 +101,20 @@ def streams(index: int) -> dict:
 # ----------------------------------------------------------------------------
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round fp32 to bf16 (nearest even) and return the raw uint16 bits."""
+    """Round fp32 to bf16 (nearest even) and return the raw uint16 bits.
+    Finite inputs cannot overflow the uint32 sum (the largest is 0xFF7FFFFF)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    out = rounded.astype(np.uint16)
-    nan = np.isnan(x)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint16)
+    step = 1 << 24
+    for o in range(0, flat.size, step):
+        u = flat[o:o + step].view(np.uint32)
+        r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+        out[o:o + step] = r.astype(np.uint16)
+    nan = np.isnan(flat)
     if nan.any():
         out[nan] = 0x7FC0
-    return out
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
@@ -282,9 +288,11 @@ class PagedLayout:
     num_pages: int            # pool size including the reserved page 0
     num_slots: int
     write_locations: np.ndarray  # int64 [B*N]: slot of window node i of request b
+    page_size: int = PAGE_SIZE
 
     def slot(self, b: int, pos: int) -> int:
-        return int(self.page_table[b, pos // PAGE_SIZE]) * PAGE_SIZE + pos % PAGE_SIZE
+        ps = self.page_size
+        return int(self.page_table[b, pos // ps]) * ps + pos % ps
 
 
 def make_prefix_lens(w: Workload, rng: np.random.Generator) -> np.ndarray:
@@ -300,8 +308,8 @@ def make_layout(w: Workload, prefix_len: np.ndarray, rng: np.random.Generator,
     window at logical positions P_b .. P_b+N-1. Physical page 0 is reserved (a
     dummy slot resolves there); the others are a seeded random permutation of
     the pool, or in order for a contiguous layout."""
-    B, N = w.B, w.N
-    need = [(int(p) + N + PAGE_SIZE - 1) // PAGE_SIZE for p in prefix_len]
+    B, N, ps = w.B, w.N, w.page_size
+    need = [(int(p) + N + ps - 1) // ps for p in prefix_len]
     total = sum(need) + extra_pages
     phys = np.arange(1, total + 1, dtype=np.int64)
     if not w.contiguous:
@@ -314,7 +322,7 @@ def make_layout(w: Workload, prefix_len: np.ndarray, rng: np.random.Generator,
         o += need[b]
     num_pages = total + 1
     wl = np.zeros(B * N, np.int64)
-    lay = PagedLayout(prefix_len.astype(np.int32), table, num_pages, num_pages * PAGE_SIZE, wl)
+    lay = PagedLayout(prefix_len.astype(np.int32), table, num_pages, num_pages * ps, wl, ps)
     for b in range(B):
         for i in range(N):
             wl[b * N + i] = lay.slot(b, int(prefix_len[b]) + i)

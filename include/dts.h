@@ -1,0 +1,271 @@
+/*
+ * dts.h - C ABI of the target-verify step of draft-tree speculative decoding,
+ * built for GB300 (sm_103a).
+ *
+ * A verify step runs the N <= 64 nodes of one draft tree per request through
+ * one target forward. This library provides that step's data-parallel path:
+ *
+ *   dts_build_tree_mask         parents/depth -> 64-bit ancestor masks,
+ *                               positions vc + depth, first-child/next-sibling
+ *   dts_write_window_kv         RoPE'd window K and V into the paged cache
+ *   dts_tree_verify_attention   every row attends the committed prefix plus
+ *                               its own ancestors; out + base-2 LSE
+ *   dts_verify_tree_greedy      greedy walk -> accept_len, packed path, tokens
+ *   dts_compact_window_rows     the path's KV rows -> the window's front slots
+ *   dts_compact_rows            the path's hidden rows -> the front; positions
+ *                               back to vc + i
+ *
+ * Sources (web pages, cited by title and section):
+ *   [TS] "Draft-tree speculation" (tokenspeed design notes)
+ *   [AK] "EAGLE Tree Attention candidate layout, positions and visibility"
+ *        (DeepSeek-V4 tree-attention source analysis)
+ *   [MI] "Medusa, EAGLE-1/2/3, MTP, and tree attention" (chapter 6.4)
+ *   [DD] "From Greedy to Sampling: The Architecture of Choice in DDTree
+ *        Speculative Decoding"
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is DEVICE memory owned by the caller, unless the
+ *     comment says otherwise. The library never allocates, frees or keeps a
+ *     pointer after the call returns.
+ *   - bf16 tensors are passed as uint16_t storage (the raw bf16 bits).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and never synchronises, so the calls can be
+ *     captured in a CUDA graph.
+ *   - The return value is a host-side status (DTS_OK or a negative
+ *     DTS_ERR_*), found before anything is launched, or DTS_ERR_CUDA if a
+ *     launch failed.
+ *   - Data errors that only the device can see (a bad parent index, a page id
+ *     out of range, ...) never trap: the kernel writes a DTS_DEV_* code to
+ *     *err_dev (an int32 in device memory; the first error wins, so the caller
+ *     zeroes it before a step and reads it when convenient) and skips the bad
+ *     item. err_dev may be NULL, in which case such errors go unreported.
+ */
+#ifndef DTS_H
+#define DTS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dts_stream_t; /* == cudaStream_t */
+
+/* host-side status codes */
+#define DTS_OK 0
+#define DTS_ERR_INVALID (-1)     /* null pointer, bad shape or alignment */
+#define DTS_ERR_UNSUPPORTED (-2) /* N > 64, d not 64/128, ... */
+#define DTS_ERR_WORKSPACE (-3)   /* workspace missing or too small */
+#define DTS_ERR_CUDA (-4)        /* a kernel launch or driver call failed */
+
+/* device-detected data errors written to *err_dev */
+#define DTS_DEV_OK 0
+#define DTS_DEV_BAD_PARENT 1   /* parents[0] != -1, or not 0 <= parents[i] < i */
+#define DTS_DEV_BAD_DEPTH 2    /* depth[0] != 0, or depth[i] != depth[parent]+1 */
+#define DTS_DEV_BAD_LINK 3     /* next_token/next_sibling out of range or cyclic */
+#define DTS_DEV_BAD_SLOT 4     /* page id, slot or prefix length out of range */
+#define DTS_DEV_BAD_PATH 5     /* accept_len / accepted_path not a valid packed path */
+#define DTS_DEV_BAD_BUFFER 6   /* a KV buffer entry is misaligned or partly overlaps another */
+#define DTS_DEV_TIMEOUT 7      /* a bounded wait inside a kernel gave up */
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int dts_version(void);
+
+/* Readable text for a DTS_* status or a DTS_DEV_* code. Static strings. */
+const char *dts_status_string(int status);
+const char *dts_device_error_string(int code);
+
+/*
+ * dts_build_tree_mask - validate B trees and derive what the verify forward
+ * and the walk need.
+ *
+ * Defined by [TS] "One tree attention" (one 64-bit ancestor mask per row),
+ * "Position follows depth, slot follows node index" (position vc + depth[i]),
+ * [AK] section one (a row sees the prefix, itself and its ancestors) and [MI]
+ * "Flattening, and the two link arrays" (first-child / next-sibling).
+ *
+ *   parents   int32 [B][N]  parents[b][0] = -1 (the root), 0 <= parents[b][i] < i
+ *   depth     int32 [B][N]  depth[b][0] = 0, depth[b][i] = depth[b][parents[b][i]] + 1
+ *   vc        int32 [B]     committed prefix length of each request
+ *   mask      u64   [B][N]  out: bit j of mask[b][i] set iff j == i or j is an
+ *                           ancestor of i
+ *   positions int32 [B][N]  out: vc[b] + depth[b][i]
+ *   next_token   int32 [B][N] out: lowest-index child of i, or -1
+ *   next_sibling int32 [B][N] out: next-higher-index child of i's parent, or -1
+ *
+ * 1 <= N <= 64, B >= 0 (B = 0 launches nothing). A request whose tree is
+ * invalid gets DTS_DEV_BAD_PARENT or DTS_DEV_BAD_DEPTH in *err_dev and all of
+ * its outputs set to 0 / -1 (mask 0, positions vc, links -1).
+ */
+int dts_build_tree_mask(const int32_t *parents, const int32_t *depth, const int32_t *vc,
+                        int B, int N, uint64_t *mask, int32_t *positions,
+                        int32_t *next_token, int32_t *next_sibling, int32_t *err_dev,
+                        dts_stream_t stream);
+
+/*
+ * dts_write_window_kv - store the window's K (rotated) and V in the paged cache.
+ *
+ * Defined by [TS] "Position follows depth, slot follows node index": node i's
+ * K/V go to the slot of logical position vc + i (slot follows node index),
+ * and K is rotated at positions[b][i] = vc + depth[i] (position follows depth).
+ * RoPE reading: rotate-half pairs (x_k, x_{k+d/2}), angle pos * theta^(-2k/d).
+ *
+ *   k_new, v_new  bf16 [B*N][Hkv][d]   the window's new keys (not rotated) and values
+ *   positions     int32 [B][N]         RoPE position of each node
+ *   page_table    int32 [B][max_pages] physical page of each logical page
+ *   prefix_len    int32 [B]            P_b = vc: node i lives at logical position P_b + i
+ *   k_cache, v_cache bf16 [num_slots][Hkv][d], slot = page * page_size + offset
+ *   write_locations int64 [B*N]        optional out (NULL = skip): the slot of each node
+ *
+ * d in {64, 128}; page_size a power of two in [8, 4096]; Hkv >= 1.
+ * A page id or slot out of range gives DTS_DEV_BAD_SLOT and skips that node.
+ */
+int dts_write_window_kv(const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
+                        const int32_t *page_table, int max_pages, int page_size,
+                        const int32_t *prefix_len, int B, int N, int Hkv, int d,
+                        int64_t num_slots, float rope_theta, uint16_t *k_cache,
+                        uint16_t *v_cache, int64_t *write_locations, int32_t *err_dev,
+                        dts_stream_t stream);
+
+/*
+ * dts_tree_verify_attention_workspace - bytes of device workspace that
+ * dts_tree_verify_attention needs for these sizes (0 never happens for B > 0).
+ * max_prefix is an upper bound on every prefix_len[b]. Host-only; no CUDA call.
+ */
+size_t dts_tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d,
+                                           int64_t max_prefix);
+
+/*
+ * dts_tree_verify_attention - attention of the N verify rows of each request.
+ *
+ * Defined by [TS] "One tree attention": every row sees the committed prefix,
+ * and the 64-bit ancestor mask applies only to the last W = N keys (the
+ * window); the result carries a base-2 log-sum-exp. [AK] section one: row v
+ * must equal Target(prefix + path(root -> v)). [AK] section four: partial
+ * results over disjoint key sets merge by their log-sum-exps.
+ *
+ *   q          bf16 [B*N][Hq][d]       queries; rotated here at positions[b][i]
+ *                                      unless positions is NULL (then taken as
+ *                                      already rotated)
+ *   k_cache, v_cache bf16 [num_slots][Hkv][d]  paged cache; prefix keys already
+ *                                      rotated; window keys written by
+ *                                      dts_write_window_kv
+ *   page_table int32 [B][max_pages]
+ *   prefix_len int32 [B]               P_b; window node j is at logical position P_b + j
+ *   max_prefix host int64              upper bound on every P_b (plans the KV split)
+ *   mask       u64 [B][N]              from dts_build_tree_mask
+ *   positions  int32 [B][N] or NULL
+ *   softmax_scale  0 -> 1/sqrt(d)
+ *   out        bf16 [B*N][Hq][d]       out: normalised attention output
+ *   lse2       fp32 [B*N][Hq]          out: log2(sum_j exp(s_j)) over the row's keys
+ *   workspace  device, >= dts_tree_verify_attention_workspace(...) bytes,
+ *              16-byte aligned; its contents on entry do not matter
+ *
+ * Query head h reads KV head h / (Hq/Hkv). d in {64, 128}; Hq % Hkv == 0;
+ * 1 <= N <= 64; page_size a power of two in [8, 4096]; cache and q base
+ * addresses 16-byte aligned. Window keys that a row's mask does not select are
+ * never read for that row (non-finite values there cannot leak). A row whose
+ * mask is 0 and whose prefix is empty gets out = 0 and lse2 = -inf.
+ * DTS_DEV_BAD_SLOT if prefix_len[b] < 0, > max_prefix, or the window runs past
+ * max_pages * page_size, or a page id is outside the pool.
+ */
+int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache,
+                              const uint16_t *v_cache, int64_t num_slots,
+                              const int32_t *page_table, int max_pages, int page_size,
+                              const int32_t *prefix_len, int64_t max_prefix,
+                              const uint64_t *mask, const int32_t *positions,
+                              float rope_theta, int B, int N, int Hq, int Hkv, int d,
+                              float softmax_scale, uint16_t *out, float *lse2,
+                              void *workspace, size_t ws_bytes, int32_t *err_dev,
+                              dts_stream_t stream);
+
+/*
+ * dts_verify_tree_greedy - greedy tree verification, one warp per request.
+ *
+ * Defined by [MI] "Walking the accepted path": from the root, descend to the
+ * first child, scan the siblings for one whose draft token equals the
+ * target's argmax at the parent, accept it and repeat; stop when no sibling
+ * matches. [AK] section two: accept_len = correct drafts + 1; the accepted
+ * outputs are the target argmax at each accepted node (the last is the bonus).
+ * [TS] "The tree is a parameter of the chain path": the path is packed.
+ *
+ *   draft_tokens, target_argmax int32 [B][N]
+ *   next_token, next_sibling    int32 [B][N]  the links (from dts_build_tree_mask),
+ *                               or both NULL to derive children from parents
+ *   parents                     int32 [B][N]  used only when the links are NULL
+ *   accept_len       int32 [B]     out: number of accepted nodes, >= 1
+ *   accepted_path    int32 [B][N]  out: accepted node ids (local), -1 padded
+ *   accepted_tokens  int32 [B][N]  out: target_argmax at each accepted node, -1 padded
+ *
+ * Siblings are scanned in link order (ascending node index when the links come
+ * from dts_build_tree_mask or from parents); the first match wins. A link out
+ * of range or a cycle gives DTS_DEV_BAD_LINK and accept_len = 1.
+ */
+int dts_verify_tree_greedy(const int32_t *draft_tokens, const int32_t *target_argmax,
+                           const int32_t *parents, const int32_t *next_token,
+                           const int32_t *next_sibling, int B, int N, int32_t *accept_len,
+                           int32_t *accepted_path, int32_t *accepted_tokens,
+                           int32_t *err_dev, dts_stream_t stream);
+
+/*
+ * One K or V buffer of one layer (an entry of a cache group's address table).
+ * Row s occupies bytes [base + s * slot_stride_bytes, ... + row_bytes).
+ */
+typedef struct dts_kv_buffer {
+  void *base;                /* device address of slot 0 */
+  int64_t slot_stride_bytes; /* bytes between consecutive slots */
+  int64_t num_slots;         /* slots in this buffer (bounds check) */
+  int32_t row_bytes;         /* bytes moved per slot; a multiple of 4 */
+  int32_t reserved;          /* must be 0 */
+} dts_kv_buffer;
+
+/*
+ * dts_compact_window_rows - move the accepted path's KV rows to the window's
+ * leading slots in every buffer of the table.
+ *
+ * Defined by [TS] "The tree is a parameter of the chain path": the path's
+ * target KV of every layer moves to the window's leading slots, by a word copy
+ * that does not care about dtype, through a K/V address table per cache
+ * group; [MI] "Discarding the rejected branches' KV": destinations are the
+ * first accept_len window slots, sources the accepted nodes' slots.
+ *
+ *   table           dts_kv_buffer [n_buffers] in DEVICE memory
+ *   write_locations int64 [B*N]   slot of window node i of request b
+ *   accepted_path   int32 [B][N], accept_len int32 [B]  (dts_verify_tree_greedy)
+ *
+ * For t < accept_len[b]: row(write_locations[b*N+t]) <- row(write_locations[
+ * b*N+path[t]]), read before anything is written (a path such as [0,2,3] reads
+ * slot 2 for t=1 before writing it for t=2). Rows with path[t] == t do not
+ * move. Each physical region moves once: an entry whose rows lie inside
+ * another entry's rows (same stride; an aliased layer or a value view of a key
+ * row) is skipped; entries that overlap only partly give DTS_DEV_BAD_BUFFER.
+ * base and slot_stride_bytes must be multiples of 4 (16 gives the vector path).
+ */
+int dts_compact_window_rows(const dts_kv_buffer *table, int n_buffers,
+                            const int64_t *write_locations, const int32_t *accepted_path,
+                            const int32_t *accept_len, int B, int N, int32_t *err_dev,
+                            dts_stream_t stream);
+
+/*
+ * dts_compact_rows - move the accepted path's hidden rows to the front of each
+ * request's window and put the positions back to vc + i.
+ *
+ * Defined by [TS] "The tree is a parameter of the chain path" (hidden rows to
+ * the front, positions from vc + depth back to vc + i) and "Position follows
+ * depth" (the two position shifts cancel for any depth).
+ *
+ *   hidden     [B*N] rows of row_bytes bytes (row_bytes a multiple of 4)
+ *   positions  int32 [B][N]   out: vc[b] + i for every i < N (may be NULL)
+ *   vc         int32 [B]
+ * For t < accept_len[b]: hidden[b*N+t] <- hidden[b*N+path[t]] (snapshot).
+ */
+int dts_compact_rows(void *hidden, int64_t row_bytes, int32_t *positions, const int32_t *vc,
+                     const int32_t *accepted_path, const int32_t *accept_len, int B, int N,
+                     int32_t *err_dev, dts_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTS_H */

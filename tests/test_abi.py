@@ -1,0 +1,68 @@
+"""The C-ABI library loads and exports every symbol include/dts.h declares.
+
+Runs without a GPU: only host-side entry points are called (version, status
+text, workspace size, argument validation that fails before any launch).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import draft_tree_speculative_gb300 as dts
+from draft_tree_speculative_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dts.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dts_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        B.build()
+    return dts.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    assert set(names) == set(dts.EXPORTED)
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_host_only_calls(lib):
+    assert dts.version() >= 100
+    assert dts.status_string(0) == "ok"
+    assert "workspace" in dts.status_string(dts.ERR_WORKSPACE)
+    assert dts.device_error_string(dts.DEV_BAD_PARENT) == "bad parent index"
+    # workspace: n_splits * B*N*Hq * (d + 1) fp32 words (each part 256-byte aligned)
+    ws = dts.tree_verify_attention_workspace(32, 64, 32, 8, 128, 8192)
+    rows = 32 * 64 * 32
+    assert ws % 256 == 0 and ws >= rows * 129 * 4
+    assert dts.tree_verify_attention_workspace(1, 5, 4, 1, 64, 0) > 0
+    assert dts.tree_verify_attention_workspace(1, 5, 4, 3, 64, 10) == 0     # Hq % Hkv != 0
+
+
+def test_validation_before_launch(lib):
+    L = dts.lib()
+    # N > 64 is unsupported; B = 0 launches nothing
+    assert L.dts_build_tree_mask(None, None, None, 1, 65, None, None, None, None, None, None) == dts.ERR_UNSUPPORTED
+    assert L.dts_build_tree_mask(None, None, None, 0, 8, None, None, None, None, None, None) == dts.OK
+    assert L.dts_build_tree_mask(None, None, None, 2, 8, None, None, None, None, None, None) == dts.ERR_INVALID
+    assert L.dts_verify_tree_greedy(None, None, None, None, None, 3, 8, None, None, None, None, None) == dts.ERR_INVALID
+    assert L.dts_compact_rows(4096, 6, None, None, None, None, 2, 8, None, None) == dts.ERR_INVALID  # row_bytes % 4
+    assert L.dts_compact_rows(None, 0, None, None, None, None, 2, 8, None, None) == dts.OK       # nothing to do
+    assert L.dts_compact_window_rows(None, 1, None, None, None, 1, 65, None, None) == dts.ERR_UNSUPPORTED
+    assert L.dts_write_window_kv(None, None, None, None, 4, 64, None, 1, 8, 8, 96, 100, 5e5, None, None, None,
+                                 None, None) == dts.ERR_UNSUPPORTED
+    assert L.dts_tree_verify_attention(None, None, None, 100, None, 4, 48, None, 0, None, None, 5e5, 1, 8, 32, 8,
+                                       128, 0.0, None, None, None, 0, None, None) == dts.ERR_UNSUPPORTED
+    assert L.dts_tree_verify_attention(None, None, None, 100, None, 4, 64, None, 0, None, None, 5e5, 1, 8, 30, 8,
+                                       128, 0.0, None, None, None, 0, None, None) == dts.ERR_INVALID

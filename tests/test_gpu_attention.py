@@ -1,0 +1,212 @@
+"""GPU parity: write_window_kv and tree_verify_attention against the oracle,
+through the C ABI, on the workloads' seeded inputs and on edge cases.
+
+Tolerances (stated in the task's target): attention output within atol 1e-2 /
+rtol 1e-2 (bf16), base-2 LSE within 1e-3 absolute.
+"""
+import numpy as np
+import pytest
+
+import draft_tree_speculative_gb300 as dts
+from draft_tree_speculative_gb300 import synth
+from draft_tree_speculative_gb300.step import DeviceBatch, run_step
+from oracle import attention as OA
+from oracle import rope as OR
+from tests.gpu_helpers import (assert_attention_close, bf16_bits_of, bf16_to_f64, custom_workload, random_tree,
+                               torch_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_attention(inp, page_poison=None, poison_nodes=()):
+    """GPU: mask -> window kv -> attention. Optional NaN poison: fills every
+    cache slot that no row may read (reserved page 0, slots past each window)
+    and the K/V of `poison_nodes` (flat b*N+i) with NaN/Inf."""
+    torch = torch_cuda()
+    if poison_nodes:
+        inp.k_new[list(poison_nodes)] = 0x7FC0
+        inp.v_new[list(poison_nodes)] = 0x7F80
+    db = DeviceBatch(inp, compact_attention_kv=False, fp8_layers=0)
+    if page_poison:
+        ps = db.page_size
+        nan = torch.tensor(0x7FC0, dtype=torch.int16).view(torch.bfloat16)
+        db.k_cache[:ps] = nan
+        db.v_cache[:ps] = nan
+        lay = inp.layout
+        for b in range(inp.w.B):
+            end = int(lay.prefix_len[b]) + inp.w.N
+            last = (end + ps - 1) // ps * ps
+            for pos in range(end, last):
+                s = lay.slot(b, pos)
+                db.k_cache[s] = nan
+                db.v_cache[s] = nan
+    db.mask_step()
+    db.window_kv_step()
+    db.attention_step()
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0
+    return db, bf16_to_f64(db.out), db.lse2.cpu().numpy().astype(np.float64)
+
+
+def _oracle(inp, rows=None):
+    w = inp.w
+    return OA.verify_attention(inp.q, inp.k_new, inp.v_new, inp.k_cache, inp.v_cache, inp.layout.page_table,
+                               inp.vc, inp.parents, w.Hkv, w.rope_theta, page_size=w.page_size, rows=rows)
+
+
+def test_write_window_kv_matches_rope():
+    torch = torch_cuda()
+    for name in ("tiny_p128_n5", "llama8b_p4096_n8"):
+        inp = synth.make_inputs(synth.WORKLOADS[name])
+        w = inp.w
+        db = DeviceBatch(inp, compact_attention_kv=False, fp8_layers=0)
+        before_k = bf16_bits_of(db.k_cache)
+        db.mask_step()
+        db.window_kv_step()
+        torch.cuda.synchronize()
+        assert int(db.err.item()) == 0
+        wl = db.write_locations.cpu().numpy()
+        assert (wl == inp.layout.write_locations).all()
+        k_after = bf16_bits_of(db.k_cache)
+        v_after = bf16_bits_of(db.v_cache)
+        pos = inp.vc[:, None].astype(np.int64) + inp.depth
+        ref = OR.rotate(synth.bf16_bits_to_f64(inp.k_new), pos.reshape(-1)[:, None], w.rope_theta)
+        got = synth.bf16_bits_to_f64(k_after[wl])
+        # one bf16 ulp of the exact rotation
+        assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6).all()
+        assert (v_after[wl] == inp.v_new).all()
+        untouched = np.ones(len(before_k), bool)
+        untouched[wl] = False
+        assert (k_after[untouched] == before_k[untouched]).all()
+
+
+@pytest.mark.parametrize("name", ["tiny_p128_n5", "llama8b_p4096_n8"])
+def test_attention_small_workloads_all_rows(name):
+    inp = synth.make_inputs(synth.WORKLOADS[name])
+    _, out, lse = _run_attention(inp)
+    ref_o, ref_l = _oracle(inp)
+    assert_attention_close(out, lse, ref_o, ref_l, range(inp.w.B * inp.w.N))
+
+
+def _sample_rows(w, parents, rng, k):
+    rows = {(0, 0), (w.B - 1, w.N - 1)}
+    deep = int(np.argmax(synth.depth_of(parents[0])))
+    rows.add((0, deep))
+    while len(rows) < k:
+        rows.add((int(rng.integers(0, w.B)), int(rng.integers(0, w.N))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name,k", [("eagle2_p8192_n64", 24), ("longctx_p131072_n64", 8), ("highconc_b128_n16", 24)])
+def test_attention_full_size_sampled_rows(name, k):
+    """Full-size workload in the launch configuration the benchmark times;
+    the oracle recomputes a sample of rows (all heads) one by one."""
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    _, out, lse = _run_attention(inp)
+    rows = _sample_rows(w, inp.parents, np.random.default_rng(7), k)
+    ref_o, ref_l = _oracle(inp, rows=rows)
+    assert_attention_close(out, lse, ref_o, ref_l, [b * w.N + v for b, v in rows])
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+EDGE = [
+    # (label, base workload, overrides, tree kind)
+    ("p0", "llama8b_p4096_n8", dict(B=2, prefix=[0, 0]), None),
+    ("p_ragged_not_multiple", "llama8b_p4096_n8", dict(B=4, prefix=[1, 63, 200, 1000]), None),
+    ("chain64", "eagle2_p8192_n64", dict(B=2, prefix=[300, 129]), "chain"),
+    ("star64", "eagle2_p8192_n64", dict(B=2, prefix=[257, 128]), "star"),
+    ("n5_random", "llama8b_p4096_n8", dict(B=3, N=5, prefix=[77, 640, 1]), "random"),
+    ("n17_random", "llama8b_p4096_n8", dict(B=3, N=17, prefix=[511, 513, 4099]), "random"),
+    ("page16", "llama8b_p4096_n8", dict(B=2, prefix=[333, 1024], page_size=16), "random"),
+    ("page128", "llama8b_p4096_n8", dict(B=2, prefix=[333, 1024], page_size=128), "random"),
+    ("d64_g1", "tiny_p128_n5", dict(B=2, Hq=2, Hkv=2, prefix=[130, 4000], contiguous=False), None),
+    ("g8_two_row_pairs", "longctx_p131072_n64", dict(B=2, prefix=[700, 2050]), None),
+    ("g2", "llama8b_p4096_n8", dict(B=2, Hq=16, Hkv=8, prefix=[1500, 10]), None),
+    ("g16", "llama8b_p4096_n8", dict(B=2, Hq=32, Hkv=2, prefix=[900, 33]), "random"),
+]
+
+
+def _edge_inputs(i, base, over, kind):
+    w = custom_workload(base, i, **over)
+    rng = np.random.default_rng(500 + i)
+    trees = None
+    if kind == "chain":
+        p, d = synth.chain_tree(w.N)
+        trees = (np.tile(p, (w.B, 1)), np.tile(d, (w.B, 1)))
+    elif kind == "star":
+        p, d = synth.star_tree(w.N)
+        trees = (np.tile(p, (w.B, 1)), np.tile(d, (w.B, 1)))
+    elif kind == "random":
+        ps, ds = zip(*[random_tree(rng, w.N) for _ in range(w.B)])
+        trees = (np.array(ps), np.array(ds))
+    return synth.make_inputs(w, trees=trees, prefix_override=w.prefix)
+
+
+@pytest.mark.parametrize("i,label,base,over,kind", [(i, *e) for i, e in enumerate(EDGE)], ids=[e[0] for e in EDGE])
+def test_attention_edge_cases(i, label, base, over, kind):
+    inp = _edge_inputs(i, base, over, kind)
+    _, out, lse = _run_attention(inp)
+    ref_o, ref_l = _oracle(inp)
+    assert_attention_close(out, lse, ref_o, ref_l, range(inp.w.B * inp.w.N))
+
+
+def test_non_finite_unseen_slots_do_not_leak():
+    """NaN/Inf in slots no row may read (the reserved page, slots past the
+    window) and in the K/V of one leaf: only the leaf's own row may change."""
+    w = custom_workload("llama8b_p4096_n8", 50, B=3, prefix=[100, 191, 4096])
+    inp = synth.make_inputs(w, prefix_override=w.prefix)
+    leaf = w.N - 1                      # depth-first numbering: the last node is a leaf
+    poisoned = [b * w.N + leaf for b in range(w.B)]
+    ref_o, ref_l = _oracle(inp)         # computed before poisoning
+    _, out, lse = _run_attention(inp, page_poison=True, poison_nodes=poisoned)
+    keep = [r for r in range(w.B * w.N) if r not in poisoned]
+    assert_attention_close(out, lse, ref_o, ref_l, keep)
+    for r in poisoned:
+        assert not np.isfinite(out[r]).all()
+
+
+def test_invalid_arguments_return_status():
+    torch = torch_cuda()
+    inp = synth.make_inputs(synth.WORKLOADS["tiny_p128_n5"])
+    db = DeviceBatch(inp, compact_attention_kv=False, fp8_layers=0)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(dts.DtsError) as e:
+        dts.tree_verify_attention(db.q, db.k_cache, db.v_cache, db.page_table, 64, db.prefix_len, db.max_prefix,
+                                  db.mask, db.positions, 5e5, db.out, db.lse2, small)
+    assert e.value.status == dts.ERR_WORKSPACE
+    with pytest.raises(dts.DtsError) as e:
+        dts.tree_verify_attention(db.q, db.k_cache, db.v_cache, db.page_table, 48, db.prefix_len, db.max_prefix,
+                                  db.mask, db.positions, 5e5, db.out, db.lse2, db.workspace)
+    assert e.value.status == dts.ERR_UNSUPPORTED
+
+
+def test_bad_prefix_len_is_reported_not_trapped():
+    torch = torch_cuda()
+    inp = synth.make_inputs(synth.WORKLOADS["tiny_p128_n5"])
+    db = DeviceBatch(inp, compact_attention_kv=False, fp8_layers=0)
+    db.mask_step()
+    db.window_kv_step()
+    bad = torch.tensor([10 ** 6], dtype=torch.int32, device="cuda")    # past the page table
+    dts.tree_verify_attention(db.q, db.k_cache, db.v_cache, db.page_table, 64, bad, 10 ** 6, db.mask,
+                              db.positions, 5e5, db.out, db.lse2,
+                              torch.empty(dts.tree_verify_attention_workspace(1, 5, 4, 1, 64, 10 ** 6) + 16,
+                                          dtype=torch.uint8, device="cuda"), err=db.err)
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == dts.DEV_BAD_SLOT
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_full_step_runs_clean_and_repeats(name):
+    """The whole step (as the benchmark runs it) leaves err at 0, and a second
+    step reproduces the first's attention output bit for bit."""
+    torch = torch_cuda()
+    inp = synth.make_inputs(synth.WORKLOADS[name])
+    db = DeviceBatch(inp)
+    run_step(db)
+    torch.cuda.synchronize()
+    first = db.out.clone()
+    run_step(db)
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0
+    assert torch.equal(first, db.out)
