@@ -45,8 +45,8 @@ ATTN_SOURCES = ("draft_tree_speculative_gb300/csrc/attention.cu", "draft_tree_sp
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="eagle2_p8192_n64", choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -234,7 +234,8 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     names = ("mask", "window_kv", "attention", "walk", "compact")
     calls = (db.mask_step, db.window_kv_step, db.attention_step, db.walk_step, db.compact_step)
-    launches_per_step = 7 if db.max_prefix > 0 else 6
+    # mask, window kv, rope_q + prefix + window/merge, walk, kv compaction, row compaction
+    launches_per_step = 8 if db.max_prefix > 0 else 7
 
     def one_step(ev=None):
         for k, c in enumerate(calls):
