@@ -25,6 +25,7 @@ EXPORTED = (
     "dts_version", "dts_status_string", "dts_device_error_string", "dts_build_tree_mask",
     "dts_write_window_kv", "dts_tree_verify_attention_workspace", "dts_tree_verify_attention",
     "dts_verify_tree_greedy", "dts_compact_window_rows", "dts_compact_rows",
+    "dts_tree_verify_attention_static_ws",
 )
 
 
@@ -51,6 +52,8 @@ _SIGS = {
     "dts_tree_verify_attention_workspace": (_SZ, [_I, _I, _I, _I, _I, _L]),
     "dts_tree_verify_attention": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I, _F,
                                        _P, _P, _P, _SZ, _P, _P]),
+    "dts_tree_verify_attention_static_ws": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I,
+                                                 _F, _P, _P, _P, _P]),
     "dts_verify_tree_greedy": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "dts_compact_window_rows": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P]),
     "dts_compact_rows": (_I, [_P, _L, _P, _P, _P, _P, _I, _I, _P, _P]),
@@ -203,6 +206,29 @@ def tree_verify_attention(q, k_cache, v_cache, page_table, page_size, prefix_len
         _ptr(prefix_len), int(max_prefix), _ptr(mask), _ptr(positions), float(rope_theta), B, N, Hq, Hkv, d,
         float(softmax_scale), _ptr(out), _ptr(lse2), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
     _raise(st, "tree_verify_attention")
+
+
+def tree_verify_attention_static_ws(q, k_cache, v_cache, page_table, page_size, prefix_len, max_prefix, mask,
+                                    positions, rope_theta, out, lse2, softmax_scale=0.0, err=None, stream=None,
+                                    N=None):
+    """tree_verify_attention with the library's own fixed device workspace, for
+    callers that cannot allocate device memory (see include/dts.h)."""
+    torch = _torch()
+    BN, Hq, d = q.shape
+    B = prefix_len.shape[0]
+    N = BN // B if N is None else N
+    Hkv = k_cache.shape[1]
+    _check(q, torch.bfloat16, (BN, Hq, d), "q")
+    _check(k_cache, torch.bfloat16, None, "k_cache")
+    _check(v_cache, torch.bfloat16, tuple(k_cache.shape), "v_cache")
+    _check(mask, _u64(), None, "mask")
+    _check(out, torch.bfloat16, (BN, Hq, d), "out")
+    _check(lse2, torch.float32, (BN, Hq), "lse2")
+    st = lib().dts_tree_verify_attention_static_ws(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(page_table), page_table.shape[1], page_size,
+        _ptr(prefix_len), int(max_prefix), _ptr(mask), _ptr(positions), float(rope_theta), B, N, Hq, Hkv, d,
+        float(softmax_scale), _ptr(out), _ptr(lse2), _ptr(err), _stream(stream))
+    _raise(st, "tree_verify_attention_static_ws")
 
 
 def verify_tree_greedy(draft_tokens, target_argmax, accept_len, accepted_path, accepted_tokens, parents=None,

@@ -1011,3 +1011,66 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   wa.scale_log2 = scale * kLog2e;
   return d == 128 ? launch_window<128>(wa, s) : launch_window<64>(wa, s);
 }
+
+// ============================================================================
+// Allocation-free variant: the workspace is a fixed device array of this file.
+//
+// Some callers cannot hand out device memory: a process that has reserved the
+// whole device for its own pool, a plugin with no access to its host's
+// allocator, or code that must not call cudaMalloc while it runs. For them the
+// workspace lives in this file-scope array instead. Every GPU that loads the
+// library keeps the array for the life of the process.
+// ============================================================================
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = size_t(64) << 20;  // 64 MiB
+__device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_ws_mutex;
+void *g_static_ws_ptr[kMaxDevices] = {};
+
+// Device address of g_static_workspace on the current device. The host-side
+// name of the array is only a stand-in; its device address has to be asked
+// for once per device, with that device current.
+void *static_workspace(int *status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = DTS_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+  if (g_static_ws_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) {
+      *status = DTS_ERR_CUDA;
+      return nullptr;
+    }
+    g_static_ws_ptr[dev] = p;
+  }
+  *status = DTS_OK;
+  return g_static_ws_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int dts_tree_verify_attention_static_ws(const uint16_t *q, const uint16_t *k_cache,
+                                                   const uint16_t *v_cache, int64_t num_slots,
+                                                   const int32_t *page_table, int max_pages, int page_size,
+                                                   const int32_t *prefix_len, int64_t max_prefix,
+                                                   const uint64_t *mask, const int32_t *positions, float rope_theta,
+                                                   int B, int N, int Hq, int Hkv, int d, float softmax_scale,
+                                                   uint16_t *out, float *lse2, int32_t *err_dev,
+                                                   dts_stream_t stream) {
+  if (B == 0) return DTS_OK;
+  const size_t need = dts_tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_prefix);
+  if (need > kStaticWorkspaceBytes) return DTS_ERR_WORKSPACE;
+  int status = DTS_OK;
+  void *ws = static_workspace(&status);
+  if (ws == nullptr) return status;
+  // No part of the workspace needs to start at zero: every byte a call reads
+  // was written earlier in the same call.
+  return dts_tree_verify_attention(q, k_cache, v_cache, num_slots, page_table, max_pages, page_size, prefix_len,
+                                   max_prefix, mask, positions, rope_theta, B, N, Hq, Hkv, d, softmax_scale, out,
+                                   lse2, ws, kStaticWorkspaceBytes, err_dev, stream);
+}

@@ -181,6 +181,35 @@ int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache,
                               dts_stream_t stream);
 
 /*
+ * dts_tree_verify_attention_static_ws - dts_tree_verify_attention without a
+ * caller-supplied workspace. The pages have no counterpart: this is a service
+ * for callers that cannot allocate device memory, such as a process whose own
+ * pool already holds the whole device, a plugin without access to its host's
+ * allocator, or code that must not call cudaMalloc while it runs.
+ *
+ * Arguments and results are those of dts_tree_verify_attention, minus
+ * workspace/ws_bytes. The scratch space is a fixed 64 MiB array in the
+ * library's device image; every GPU that loads the library holds it until the
+ * process exits. Shapes whose workspace (dts_tree_verify_attention_workspace)
+ * exceeds 64 MiB get DTS_ERR_WORKSPACE and nothing runs.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture. The call allocates and frees nothing.
+ * All calls share the one array: calls whose work overlaps on the GPU (other
+ * streams, other host threads) race and give wrong results, so serialise them.
+ * Nothing in the array needs clearing between calls.
+ */
+int dts_tree_verify_attention_static_ws(const uint16_t *q, const uint16_t *k_cache,
+                                        const uint16_t *v_cache, int64_t num_slots,
+                                        const int32_t *page_table, int max_pages, int page_size,
+                                        const int32_t *prefix_len, int64_t max_prefix,
+                                        const uint64_t *mask, const int32_t *positions,
+                                        float rope_theta, int B, int N, int Hq, int Hkv, int d,
+                                        float softmax_scale, uint16_t *out, float *lse2,
+                                        int32_t *err_dev, dts_stream_t stream);
+
+/*
  * dts_verify_tree_greedy - greedy tree verification, one warp per request.
  *
  * Defined by [MI] "Walking the accepted path": from the root, descend to the
