@@ -104,6 +104,27 @@ def recorded_traffic(workload):
 
 
 # ----------------------------------------------------------------------------
+# replicas: the slowest rank's time, whole-job throughput
+# ----------------------------------------------------------------------------
+
+def reduce_max(x: float, device) -> float:
+    """Max of x over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rows_per_s(rows_per_step_per_rank: int, world: int, slowest_ms_per_step: float) -> float:
+    """Every rank runs its own replica, so the job's rows per step are world x
+    one replica's, and the job is as fast as its slowest rank."""
+    return world * rows_per_step_per_rank / (slowest_ms_per_step / 1e3)
+
+
+# ----------------------------------------------------------------------------
 # clocks during the timed region
 # ----------------------------------------------------------------------------
 
@@ -272,14 +293,10 @@ def run_ours(args, rank, world, local_rank):
         step_ms.append(ev[0].elapsed_time(ev[-1]))
         for k, n in enumerate(names):
             per_call[n].append(ev[k].elapsed_time(ev[k + 1]))
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     rows_per_step = w.B * w.N
-    value = world * rows_per_step / (ms_per_step / 1e3)
+    value = whole_job_rows_per_s(rows_per_step, world, ms_per_step)
 
     # roofline of the attention call (prefix pass + window/merge pass)
     attn_ms = statistics.mean(per_call["attention"])
@@ -323,12 +340,8 @@ def run_ours(args, rank, world, local_rank):
                 if s >= args.warmup:
                     ev[s - args.warmup][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = sum(a.elapsed_time(b) for a, b in ev)
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * rows_per_step / (e_ms / args.steps / 1e3), "unit": "rows/s",
+        e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), dev)
+        e2e = {"value": whole_job_rows_per_s(rows_per_step, world, e_ms / args.steps), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     assert int(db.err.item()) == 0, "device reported an error"
 
