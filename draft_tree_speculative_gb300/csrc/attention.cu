@@ -377,23 +377,31 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t kIdescO = idesc_bf16(128, D, true);
       auto slot_of = [](int use) { return use % kSlots; };
       auto phase_of = [](int use) { return static_cast<uint32_t>(use / kSlots) & 1u; };
+      // One thread issues every MMA, so the issue loop must stay short: the
+      // descriptors are built once and only their 16-byte start-address field
+      // (bits 0-13) moves, by compile-time offsets, between MMAs.
+      const uint64_t q_desc0 = sdesc_sw128(sQ_addr, 16, 1024);                // K-major Q tiles
+      const uint64_t k_desc0 = sdesc_sw128(sKV_addr, 16, 1024);               // K-major K tiles
+      const uint64_t v_desc0 = sdesc_sw128(sKV_addr, S::kBlockBytes, 1024);   // MN-major V tiles
+      constexpr uint64_t kTileStep = kTileBytes >> 4;
       auto issue_s = [&](int t, int slot) {
-        const uint32_t qa = sQ_addr + t * kTileBytes;
-        const uint32_t kb = sKV_addr + slot * kTileBytes;
+        const uint64_t qa = q_desc0 + static_cast<uint64_t>(t) * kTileStep;
+        const uint64_t kb = k_desc0 + static_cast<uint64_t>(slot) * kTileStep;
+        const uint32_t d_tmem = tmem + t * 256;
 #pragma unroll
         for (int ks = 0; ks < kKSteps; ++ks) {
-          const uint32_t off = (ks >> 2) * S::kBlockBytes + (ks & 3) * 32;
-          mma_ss(tmem + t * 256, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescS,
-                 ks > 0 ? 1u : 0u);
+          const uint64_t off = ((ks >> 2) * S::kBlockBytes + (ks & 3) * 32) >> 4;
+          mma_ss(d_tmem, qa + off, kb + off, kIdescS, ks > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int slot, bool first) {
-        const uint32_t vb = sKV_addr + slot * kTileBytes;
+        const uint64_t vb = v_desc0 + static_cast<uint64_t>(slot) * kTileStep;
+        const uint32_t d_tmem = tmem + t * 256 + 128;
+        const uint32_t p_tmem = tmem + t * 256;
+        const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 128 keys, 16 per step
-          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + ks * 8,
-                 sdesc_sw128(vb + ks * 2048, S::kBlockBytes, 1024), kIdescO, (first && ks == 0) ? 0u : 1u);
-        }
+        for (int ks = 0; ks < 8; ++ks)  // 128 keys, 16 per step (2048 bytes of V)
+          mma_ts(d_tmem, p_tmem + ks * 8, vb + static_cast<uint64_t>(ks) * (2048 >> 4), kIdescO, ks == 0 ? acc0 : 1u);
       };
       int use = 0, segc = 0;
       int tcnt[2] = {0, 0}, scnt[2] = {0, 0};
@@ -407,21 +415,30 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          for (int t = 0; t < nt; ++t) {
-            issue_s(t, slot_of(use));
-            mma_commit(&s_full[t]);
+          // (row-tile loops run over the constant 2 so that per-tile counters
+          // stay in registers)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t < nt) {
+              issue_s(t, slot_of(use));
+              mma_commit(&s_full[t]);
+            }
           }
           if (nkt == 1) mma_commit(q_empty);  // the segment's last S reads Q
           mma_commit(&empty[slot_of(use)]);
         }
         __syncwarp();
+        // The tensor core takes about one group of MMAs at a time, so any work
+        // between two issue calls leaves it idle. Per row tile all waits come
+        // first; then PV_t(j) and S_t(j+1) go out back to back from one lane.
         for (int j = 0; j < nkt && ok; ++j) {
           const int vuse = use + 2 * j + 1;
           const int vslot = slot_of(vuse);
-          if (!mbar_wait(&full[vslot], phase_of(vuse), abort_flag)) {
-            ok = false;
-            break;
-          }
+          const int kuse = use + 2 * (j + 1);
+          const bool more = j + 1 < nkt;
+          ok = mbar_wait(&full[vslot], phase_of(vuse), abort_flag) &&
+               (!more || mbar_wait(&full[slot_of(kuse)], phase_of(kuse), abort_flag));
+          if (!ok) break;
           const int nvalid = min(128, sg.P - (sg.lt0 + j) * 128);
           if (nvalid < 128) {
             // keys past the prefix's end: zero their V rows so that 0 * (stale or
@@ -435,7 +452,9 @@ __global__ void __launch_bounds__(384, 1)
             fence_proxy_async();
             __syncwarp();
           }
-          for (int t = 0; t < nt && ok; ++t) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= nt) break;
             ok = mbar_wait(&p_full[t], static_cast<uint32_t>(tcnt[t] + j) & 1u, abort_flag);
             // the first PV of a segment overwrites O: the previous epilogue must have read it
             if (ok && j == 0 && scnt[t] > 0)
@@ -444,35 +463,28 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             if (lane == 0) {
               issue_pv(t, vslot, j == 0);
+              if (more) issue_s(t, slot_of(kuse));  // overwrites P_t(j) only after PV_t(j) read it
               if (t == nt - 1) mma_commit(&empty[vslot]);
-              if (j == nkt - 1) mma_commit(&o_fin[t]);
-            }
-            __syncwarp();
-            if (j + 1 < nkt) {
-              const int kuse = use + 2 * (j + 1);
-              if (t == 0) {
-                if (!mbar_wait(&full[slot_of(kuse)], phase_of(kuse), abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
-              if (lane == 0) {
-                issue_s(t, slot_of(kuse));
+              if (more) {
                 mma_commit(&s_full[t]);
                 if (t == nt - 1) {
                   if (j + 2 == nkt) mma_commit(q_empty);
                   mma_commit(&empty[slot_of(kuse)]);
                 }
+              } else {
+                mma_commit(&o_fin[t]);
               }
-              __syncwarp();
             }
+            __syncwarp();
           }
         }
         use += 2 * nkt;
-        for (int t = 0; t < nt; ++t) {
-          tcnt[t] += nkt;
-          scnt[t] += 1;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t < nt) {
+            tcnt[t] += nkt;
+            scnt[t] += 1;
+          }
         }
         ++segc;
       }
