@@ -85,25 +85,28 @@ struct RopeQArgs {
   const uint16_t *q;
   const int32_t *positions;
   uint16_t *q_rot;
-  int rows, Hq;  // rows = B*N nodes
+  int rows, Hq, heads_per_thread;  // rows = B*N nodes
   dts::RopeFreqs freqs;
 };
 
-// One thread per (node, 8-element chunk of the first half): the chunk's eight
-// angles are computed once and applied to every query head of the node.
+// One thread per (node, group of heads, 8-element chunk of the first half):
+// the chunk's eight angles are computed once and applied to the group's heads.
+// Consecutive threads take consecutive chunks of a row (coalesced 16-byte loads).
 template <int D>
 __global__ void __launch_bounds__(256) rope_q_kernel(const __grid_constant__ RopeQArgs a) {
   constexpr int kChunks = D / 16;
+  const int hgroups = a.Hq / a.heads_per_thread;
   const int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (it >= static_cast<int64_t>(a.rows) * kChunks) return;
+  if (it >= static_cast<int64_t>(a.rows) * hgroups * kChunks) return;
   const int c = static_cast<int>(it % kChunks);
-  const int64_t node = it / kChunks;
+  const int hg = static_cast<int>((it / kChunks) % hgroups);
+  const int64_t node = it / (static_cast<int64_t>(kChunks) * hgroups);
   const int pos = a.positions[node];
   float sn[8], cs[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) dts::rope_sincos(pos, a.freqs.w[8 * c + e], &sn[e], &cs[e]);
-#pragma unroll 4
-  for (int h = 0; h < a.Hq; ++h) {
+  for (int hh = 0; hh < a.heads_per_thread; ++hh) {
+    const int h = hg * a.heads_per_thread + hh;
     const int64_t off = (node * a.Hq + h) * D + 8 * c;
     uint4 x1 = *reinterpret_cast<const uint4 *>(a.q + off);
     uint4 x2 = *reinterpret_cast<const uint4 *>(a.q + off + D / 2);
@@ -775,30 +778,64 @@ __global__ void __launch_bounds__(256) tree_window_kernel(const __grid_constant_
   uint64_t mk = a.mask[node];
   if (a.N < 64) mk &= (1ull << a.N) - 1;
   const int64_t pt_row = static_cast<int64_t>(b) * a.max_pages;
+  // Ancestors go four at a time: their K/V rows are all in flight together,
+  // and the four dot products of each head reduce across the warp side by side.
+  constexpr int kBatch = 4;
   while (mk) {
-    const int j = __ffsll(static_cast<long long>(mk)) - 1;
-    mk &= mk - 1;
-    const int64_t logical = static_cast<int64_t>(P) + j;
-    const int pid = a.page_table[pt_row + (logical >> a.page_shift)];
-    const int64_t slot = static_cast<int64_t>(pid) * ps + (logical & (ps - 1));
-    if (pid < 0 || slot >= a.num_slots) {
-      if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
-      continue;
+    float kx[kBatch][E], vx[kBatch][E];
+    bool have[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      have[k] = false;
+      if (mk) {
+        const int j = __ffsll(static_cast<long long>(mk)) - 1;
+        mk &= mk - 1;
+        const int64_t logical = static_cast<int64_t>(P) + j;
+        const int pid = a.page_table[pt_row + (logical >> a.page_shift)];
+        const int64_t slot = static_cast<int64_t>(pid) * ps + (logical & (ps - 1));
+        if (pid < 0 || slot >= a.num_slots) {
+          if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
+        } else {
+          load_row<D>(a.k_cache + (slot * a.Hkv + hkv) * D, lane, kx[k]);
+          load_row<D>(a.v_cache + (slot * a.Hkv + hkv) * D, lane, vx[k]);
+          have[k] = true;
+        }
+      }
     }
-    float kx[E], vx[E];
-    load_row<D>(a.k_cache + (slot * a.Hkv + hkv) * D, lane, kx);
-    load_row<D>(a.v_cache + (slot * a.Hkv + hkv) * D, lane, vx);
 #pragma unroll
     for (int u = 0; u < HW; ++u) {
-      float d = 0.f;
+      float s[kBatch];
 #pragma unroll
-      for (int e = 0; e < E; ++e) d = fmaf(q[u][e], kx[e], d);
-      const float s2 = warp_sum(d) * a.scale_log2;
-      const float mn = fmaxf(m[u], s2);
-      const float sa = dts::ptx::ex2(m[u] - mn), sb = dts::ptx::ex2(s2 - mn);
+      for (int k = 0; k < kBatch; ++k) {
+        float d = 0.f;
+        if (have[k]) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[u][e] = acc[u][e] * sa + vx[e] * sb;
-      l[u] = l[u] * sa + sb;
+          for (int e = 0; e < E; ++e) d = fmaf(q[u][e], kx[k][e], d);
+        }
+        s[k] = d;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], o);
+      float mn = m[u];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        s[k] *= a.scale_log2;
+        if (have[k]) mn = fmaxf(mn, s[k]);
+      }
+      const float sa = mn == -INFINITY ? 1.f : dts::ptx::ex2(m[u] - mn);  // -inf: nothing seen yet
+      l[u] *= sa;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[u][e] *= sa;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (!have[k]) continue;
+        const float w = dts::ptx::ex2(s[k] - mn);
+        l[u] += w;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[u][e] = fmaf(vx[k][e], w, acc[u][e]);
+      }
       m[u] = mn;
     }
   }
@@ -946,8 +983,9 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
     ra.q_rot = q_rot;
     ra.rows = B * N;
     ra.Hq = Hq;
+    ra.heads_per_thread = (Hq % 4 == 0) ? 4 : (Hq % 2 == 0) ? 2 : 1;
     dts_host::make_rope_freqs(rope_theta, d, &ra.freqs);
-    const int64_t items = static_cast<int64_t>(B) * N * (d / 16);
+    const int64_t items = static_cast<int64_t>(B) * N * (Hq / ra.heads_per_thread) * (d / 16);
     const int blocks = static_cast<int>((items + 255) / 256);
     if (d == 128) rope_q_kernel<128><<<blocks, 256, 0, s>>>(ra);
     else rope_q_kernel<64><<<blocks, 256, 0, s>>>(ra);
@@ -1015,7 +1053,8 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   wa.rt = plan.rt;
   wa.n_pairs = plan.n_pairs;
   wa.slot_rows = plan.slot_rows;
-  wa.heads_per_warp = (g % 8 == 0) ? 8 : (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
+  // at most 4 heads per warp: more warps in flight beat re-reading a few window rows
+  wa.heads_per_warp = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
   wa.max_pages = max_pages;
   wa.page_shift = page_shift;
   wa.grid = grid;
