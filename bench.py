@@ -1,8 +1,8 @@
 """Benchmark of one full target-verify step of draft-tree speculative decoding.
 
 A step is one pass of the whole hot path over one synthetic batch:
-build_tree_mask -> write_window_kv -> tree_verify_attention (prefix pass +
-window/merge pass) -> verify_tree_greedy -> compact_window_rows ->
+build_tree_mask -> write_window_kv -> tree_verify_attention (prep pass +
+tree attention pass) -> verify_tree_greedy -> compact_window_rows ->
 compact_rows. Inputs are resident in HBM when the timed region starts; L2 is
 flushed (512 MiB write) before every timed step, outside the step's events.
 
@@ -101,6 +101,13 @@ def recorded_traffic(workload):
     if not e or e.get("source_hash") != attention_source_hash():
         return None
     return e.get("bytes_per_call")
+
+
+def check_device_error(db, when):
+    from draft_tree_speculative_gb300 import device_error_string
+    code = int(db.err.item())
+    if code:
+        raise RuntimeError(f"device reported error {code} during {when}: {device_error_string(code)}")
 
 
 # ----------------------------------------------------------------------------
@@ -255,8 +262,8 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     names = ("mask", "window_kv", "attention", "walk", "compact")
     calls = (db.mask_step, db.window_kv_step, db.attention_step, db.walk_step, db.compact_step)
-    # mask, window kv, rope_q + prefix + window/merge, walk, kv compaction, row compaction
-    launches_per_step = 8 if db.max_prefix > 0 else 7
+    # mask, window kv, attention prep + tree attention, walk, kv compaction, row compaction
+    launches_per_step = 7
 
     def one_step(ev=None):
         for k, c in enumerate(calls):
@@ -271,7 +278,7 @@ def run_ours(args, rank, world, local_rank):
             flush.fill_(1)
             one_step()
     torch.cuda.synchronize()
-    assert int(db.err.item()) == 0, "device reported an error during warm-up"
+    check_device_error(db, "warm-up")
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
     if world > 1:
@@ -298,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
     rows_per_step = w.B * w.N
     value = whole_job_rows_per_s(rows_per_step, world, ms_per_step)
 
-    # roofline of the attention call (prefix pass + window/merge pass)
+    # roofline of the attention call (prep pass + tree attention pass)
     attn_ms = statistics.mean(per_call["attention"])
     bytes_, flops = attention_work(inp)
     hbm, tf_burst, tf_sus, src = load_peaks()
@@ -310,7 +317,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": flops / (attn_ms / 1e3) / 1e12, "peak": tf_sus, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(args.workload)
-    roof["kernel"] = "tree_verify_attention (tree_prefix_kernel + tree_window_kernel)"
+    roof["kernel"] = "tree_verify_attention (attn_prep_kernel + tree_prefix_kernel)"
     roof["algorithmic_bytes"] = bytes_
     roof["algorithmic_flops"] = flops
     roof["peak_source"] = f"{src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})"
@@ -343,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
         e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), dev)
         e2e = {"value": whole_job_rows_per_s(rows_per_step, world, e_ms / args.steps), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    assert int(db.err.item()) == 0, "device reported an error"
+    check_device_error(db, "the timed steps")
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,

@@ -10,31 +10,32 @@
 //
 // Three kernels per call:
 //
-// 0. rope_q: rotates every query row once at its node's position and stores
-//    it in bf16 (the model dtype) in the workspace.
+// 0. prep: rotates every query row once at its node's position and stores it
+//    in bf16 (the model dtype) in the workspace; writes NaN rows (and reports)
+//    for requests whose prefix length is out of range.
 //
-// 1. prefix pass (tcgen05, persistent): the rows of a KV head are the N*g
+// 1. tree attention (tcgen05, persistent): the rows of a KV head are the N*g
 //    (node, query head) pairs; a "unit" is (request, KV head, pair of 128-row
-//    tiles), and its work is the ceil(P/128) key tiles of the request's prefix.
-//    All units' key tiles form one flat sequence which the grid (one CTA per
-//    SM) splits into equal contiguous ranges, so every SM gets the same work
-//    whatever the prefix lengths. A CTA walks its range as segments (a unit's
-//    tiles inside the range). Per segment, TMA brings the unit's Q tiles and
-//    128-key K and V tiles (128-byte swizzle, one box per page and 64-column
-//    block) into shared memory; one thread issues S = Q K^T into tensor memory;
-//    each 128-thread softmax group owns one row tile (thread = TMEM lane =
-//    row), turns S into bf16 P in place (P aliases the first half of S's
-//    columns) and the MMA thread issues O += P V with P read from TMEM. The
-//    running max is rescaled lazily (only when it grows by more than 2^8).
-//    Each segment ends with a normalised fp32 partial O and its base-2 LSE
-//    written to slot (unit + CTA index) of the workspace.
+//    tiles), and its keys are the P prefix keys followed by the N window keys
+//    (the paged cache holds both), ceil((P + N)/128) key tiles. All units' key
+//    tiles form one flat sequence which the grid (one CTA per SM) splits into
+//    equal contiguous ranges, so every SM gets the same work whatever the
+//    prefix lengths. A CTA walks its range as segments (a unit's tiles inside
+//    the range). Per segment, TMA brings the unit's Q tiles and 128-key K and
+//    V tiles (128-byte swizzle, one box per page and 64-column block) into
+//    shared memory; one thread issues S = Q K^T into tensor memory; each
+//    128-thread softmax group owns one row tile (thread = TMEM lane = row),
+//    masks the window keys that are not the row's ancestors, turns S into
+//    bf16 P in place (P aliases the first half of S's columns) and the MMA
+//    thread issues O += P V with P read from TMEM. The running max is rescaled
+//    lazily (only when it grows by more than 2^8).
+//    A unit inside one segment writes its bf16 rows and base-2 LSEs directly.
+//    Otherwise every segment writes a normalised fp32 partial O and its LSE
+//    to slot (unit + CTA index).
 //
-// 2. window + merge pass (SIMT): one warp per (node, KV head, head group).
-//    It merges the unit's prefix segments by their LSEs (the CTAs that own the
-//    unit's first and last tile bound them), then walks the set bits of the
-//    node's ancestor mask (only those window keys are ever read, so
-//    non-finite values in unseen slots cannot leak), and writes bf16 out and
-//    the fp32 base-2 LSE.
+// 2. merge (SIMT): for the units split over several CTAs, one warp per 8 rows
+//    merges the partials by their LSEs (the CTAs that own the unit's first
+//    and last tile bound them) and writes bf16 out and the fp32 base-2 LSE.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -79,13 +80,19 @@ Plan make_plan(int B, int N, int Hq, int Hkv, int d) {
 }
 
 // ============================================================================
-// rope_q: q_rot[node][h] = bf16(RoPE(q[node][h], positions[node]))
+// prep: q_rot[node][h] = bf16(RoPE(q[node][h], positions[node])); NaN rows for
+// out-of-range prefix lengths
 // ============================================================================
-struct RopeQArgs {
+struct PrepArgs {
   const uint16_t *q;
-  const int32_t *positions;
+  const int32_t *positions;  // null: no rotation (q is used as given)
+  const int32_t *prefix_len;
   uint16_t *q_rot;
-  int rows, Hq, heads_per_thread;  // rows = B*N nodes
+  uint16_t *out;
+  float *lse2;
+  int32_t *err;
+  int64_t max_prefix, capacity;  // capacity: page-table rows x page size
+  int rows, N, Hq, heads_per_thread;      // rows = B*N nodes
   dts::RopeFreqs freqs;
 };
 
@@ -93,7 +100,7 @@ struct RopeQArgs {
 // the chunk's eight angles are computed once and applied to the group's heads.
 // Consecutive threads take consecutive chunks of a row (coalesced 16-byte loads).
 template <int D>
-__global__ void __launch_bounds__(256) rope_q_kernel(const __grid_constant__ RopeQArgs a) {
+__global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ PrepArgs a) {
   constexpr int kChunks = D / 16;
   const int hgroups = a.Hq / a.heads_per_thread;
   const int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -101,6 +108,22 @@ __global__ void __launch_bounds__(256) rope_q_kernel(const __grid_constant__ Rop
   const int c = static_cast<int>(it % kChunks);
   const int hg = static_cast<int>((it / kChunks) % hgroups);
   const int64_t node = it / (static_cast<int64_t>(kChunks) * hgroups);
+  const int64_t b = node / a.N;
+  const int P = a.prefix_len[b];
+  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.N > a.capacity) {
+    // the attention pass skips this request: its rows read NaN
+    if (c == 0 && hg == 0 && node == b * a.N) dts::report(a.err, DTS_DEV_BAD_SLOT);
+    const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+    for (int hh = 0; hh < a.heads_per_thread; ++hh) {
+      const int h = hg * a.heads_per_thread + hh;
+      const int64_t off = (node * a.Hq + h) * D + 8 * c;
+      *reinterpret_cast<uint4 *>(a.out + off) = nan4;
+      *reinterpret_cast<uint4 *>(a.out + off + D / 2) = nan4;
+      if (c == 0) a.lse2[node * a.Hq + h] = __int_as_float(0x7FC00000);
+    }
+    return;
+  }
+  if (a.positions == nullptr) return;
   const int pos = a.positions[node];
   float sn[8], cs[8];
 #pragma unroll
@@ -126,14 +149,17 @@ __global__ void __launch_bounds__(256) rope_q_kernel(const __grid_constant__ Rop
 }
 
 // ============================================================================
-// prefix pass
+// tree attention
 // ============================================================================
 struct PrefixArgs {
   const int32_t *page_table;
   const int32_t *prefix_len;
+  const uint64_t *mask;
   float *o_part;
   float *lse_part;
   int64_t *tiles_before;  // [B + 1], written by CTA 0 for the merge pass
+  uint16_t *out;
+  float *lse2;
   int32_t *err;
   int64_t num_slots, max_prefix;
   int B, N, Hq, Hkv, g, M, rt, npt, n_pairs, slot_rows, max_pages, page_shift;
@@ -147,21 +173,25 @@ struct PrefixShape {
   static constexpr uint32_t kBlockBytes = 128 * 128;   // one 64-column block of a 128-row tile
   static constexpr int kSlots = D == 128 ? 5 : 8;      // K/V ring
   static constexpr uint32_t kBarBytes = 512;
+  // kfull, vfull, empty, vready rings, 12 single barriers, the poison mask,
+  // the tile total (two words) and the TMEM address / abort flag words
+  static_assert((4 * kSlots + 12) * 8 + 8 + 16 + 8 <= kBarBytes, "barrier area too small");
   static constexpr uint32_t kSmem = 1024 /*align*/ + 2 * kTileBytes + kSlots * kTileBytes + kBarBytes;
 };
 
-// Key tiles of one unit of request b (0 for an empty or invalid prefix; the
-// merge pass reports the invalid ones).
+// Key tiles of one unit of request b: prefix and window keys together (0 for
+// a prefix length out of range; the prep kernel reports those).
 __device__ __forceinline__ int request_tiles(const int32_t *prefix_len, int b, int64_t max_prefix, int N,
                                              int max_pages, int page_shift) {
   const int P = prefix_len[b];
-  if (P <= 0 || P > max_prefix || static_cast<int64_t>(P) + N > (static_cast<int64_t>(max_pages) << page_shift))
+  if (P < 0 || P > max_prefix || static_cast<int64_t>(P) + N > (static_cast<int64_t>(max_pages) << page_shift))
     return 0;
-  return (P + 127) >> 7;
+  return (P + N + 127) >> 7;
 }
 
 struct Segment {
-  int b, hkv, pair, unit, lt0, lt1, P, nt;
+  int b, hkv, pair, unit, lt0, lt1, P, nt, nkt;
+  int64_t start;  // flat index of the unit's first key tile
 };
 
 // Walks the flat key-tile range [x, x1) as segments, in order.
@@ -192,6 +222,8 @@ struct SegmentWalker {
     s.hkv = uir / a.n_pairs;
     s.pair = uir - s.hkv * a.n_pairs;
     s.unit = static_cast<int>(static_cast<int64_t>(b) * per_req + uir);
+    s.nkt = nkt;
+    s.start = tb + static_cast<int64_t>(uir) * nkt;
     s.lt0 = static_cast<int>(off - static_cast<int64_t>(uir) * nkt);
     s.lt1 = static_cast<int>(min(static_cast<int64_t>(nkt), s.lt0 + (x1 - x)));
     s.P = a.prefix_len[b];
@@ -201,6 +233,74 @@ struct SegmentWalker {
     return true;
   }
 };
+
+// Visibility of 32 consecutive keys to a row whose ancestor mask is mrow
+// (bits >= N clear): bit k covers the key with window index o + k, i.e. a
+// prefix key when o + k < 0 (always seen) and window key o + k otherwise
+// (seen when that bit of mrow is set).
+__device__ __forceinline__ uint32_t visible_word(int o, uint64_t mrow) {
+  if (o <= -32) return ~0u;
+  if (o >= 64) return 0u;
+  if (o >= 0) return static_cast<uint32_t>(mrow >> o);
+  return static_cast<uint32_t>(mrow << -o) | ((1u << -o) - 1u);
+}
+
+// Phase of use u on a barrier that only the slot's uses of u's kind (K: even
+// uses, V: odd ones) complete: with an even ring a slot holds the same kind
+// every round, with an odd ring every other round.
+template <int kSlots>
+__device__ __forceinline__ uint32_t kind_phase(int use) {
+  const int round = use / kSlots;
+  return static_cast<uint32_t>(kSlots % 2 == 0 ? round : round >> 1) & 1u;
+}
+
+// Prepares the V tile of a tile that reaches the window (keys kbase ..
+// kbase + 127, window index o = kbase - P of its first key) before any PV
+// reads it, and returns the window keys whose V rows were not finite (as a
+// mask over window indices, the same in every lane). Keys past the window's
+// end get zero V rows, so that 0 * (stale or non-finite V) cannot reach O.
+// Window keys are masked per row, so a row that does not see key x still
+// multiplies P = 0 by x's V row: a non-finite V row there is zeroed and its
+// key reported, and only the rows that see it turn NaN. Kept out of line so
+// that the MMA warp's issue loop keeps its registers.
+template <int D>
+__device__ __forceinline__ uint64_t clean_window_v(uint8_t *vt, int o, int N, int lane) {
+  constexpr uint32_t kBlockBytes = 128 * 128;
+  const int nvalid = min(128, N - o);  // rows holding prefix or window keys
+  for (int h = 0; h < D / 64; ++h) {
+    uint4 *p = reinterpret_cast<uint4 *>(vt + h * kBlockBytes + nvalid * 128);
+    const int n16 = (128 - nvalid) * 8;
+    for (int e = lane; e < n16; e += 32) p[e] = make_uint4(0, 0, 0, 0);
+  }
+  uint64_t bad_keys = 0;
+  for (int x = max(-o, 0) + lane; x < nvalid; x += 32) {
+    bool bad = false;
+    for (int h = 0; h < D / 64; ++h) {
+      const uint4 *p = reinterpret_cast<const uint4 *>(vt + h * kBlockBytes + x * 128);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint4 v = p[e];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int f = 0; f < 4; ++f)
+          bad |= ((w[f] & 0x7F80u) == 0x7F80u) || ((w[f] & 0x7F800000u) == 0x7F800000u);
+      }
+    }
+    if (bad) {
+      for (int h = 0; h < D / 64; ++h) {
+        uint4 *p = reinterpret_cast<uint4 *>(vt + h * kBlockBytes + x * 128);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[e] = make_uint4(0, 0, 0, 0);
+      }
+      bad_keys |= 1ull << (o + x);
+    }
+  }
+  fence_proxy_async();  // the zeroed rows are read by the tensor core
+  __syncwarp();
+  const uint32_t lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bad_keys));
+  const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bad_keys >> 32));
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -218,22 +318,30 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t *sQ = smem;
   uint8_t *sKV = smem + 2 * kTileBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sKV + kSlots * kTileBytes);
-  uint64_t *full = bars;
-  uint64_t *empty = bars + kSlots;
-  uint64_t *s_full = bars + 2 * kSlots;
+  // The ring's slots hold K and V tiles in turn (use u: K when even, V when
+  // odd). A load completes on kfull or vfull by its kind, so each of those
+  // barriers is waited by one role only, at consecutive phases.
+  uint64_t *kfull = bars;
+  uint64_t *vfull = bars + kSlots;
+  uint64_t *empty = bars + 2 * kSlots;
+  uint64_t *s_full = bars + 3 * kSlots;
   uint64_t *p_full = s_full + 2;
   uint64_t *o_fin = p_full + 2;
   uint64_t *o_free = o_fin + 2;
   uint64_t *q_full = o_free + 2;
   uint64_t *q_empty = q_full + 1;
   uint64_t *drain = q_empty + 1;
-  int64_t *range = reinterpret_cast<int64_t *>(drain + 1);  // [0] = total tiles
+  uint64_t *win_bar = drain + 1;                             // the segment's poisoned-key mask is written
+  uint64_t *vready = win_bar + 1;                            // [kSlots] a V tile landed and is clean
+  uint64_t *poison = vready + kSlots;                        // window keys whose V rows were not finite
+  int64_t *range = reinterpret_cast<int64_t *>(poison + 1);  // [0] = total tiles
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(range + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&kfull[s], 1);
+      mbar_init(&vfull[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -245,6 +353,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(drain, 1);
+    mbar_init(win_bar, 1);
+    for (int s2 = 0; s2 < kSlots; ++s2) mbar_init(&vready[s2], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -266,7 +376,7 @@ __global__ void __launch_bounds__(384, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 2 && blockIdx.x == 0 && lane == 0) {
+  if (warp == 3 && blockIdx.x == 0 && lane == 0) {
     // tiles-before table for the merge pass
     int64_t acc = 0;
     for (int b = 0; b < a.B; ++b) {
@@ -340,7 +450,7 @@ __global__ void __launch_bounds__(384, 1)
         ++segc;
         for (int lt = sg.lt0; lt < sg.lt1 && ok; ++lt) {
           const int kbase = lt * 128;
-          const int nvalid = min(128, sg.P - kbase);
+          const int nvalid = min(128, sg.P + a.N - kbase);
           int nbox = 0;
           for (int r = 0; r < boxes; ++r) nbox += box_slot(kbase, nvalid, r) >= 0 ? 1 : 0;
           for (int kv = 0; kv < 2; ++kv, ++use) {
@@ -350,16 +460,16 @@ __global__ void __launch_bounds__(384, 1)
               ok = false;
               break;
             }
+            uint64_t *done = kv == 0 ? &kfull[slot] : &vfull[slot];
             if (lane == 0)  // the barrier expects exactly the bytes of the boxes issued below
-              mbar_expect_tx(&full[slot], static_cast<uint32_t>(nbox * rows_per_box * 128 * (D / 64)));
+              mbar_expect_tx(done, static_cast<uint32_t>(nbox * rows_per_box * 128 * (D / 64)));
             const CUtensorMap *map = kv == 0 ? &tm_k : &tm_v;
             const uint32_t dst = sKV_addr + slot * kTileBytes;
             for (int r = 0; r < boxes; ++r) {
               const int s0 = box_slot(kbase, nvalid, r);
               if (s0 < 0 || lane != 0) continue;
               for (int h = 0; h < D / 64; ++h)
-                tma_load_3d(dst + h * S::kBlockBytes + r * rows_per_box * 128, map, h * 64, sg.hkv, s0,
-                            &full[slot]);
+                tma_load_3d(dst + h * S::kBlockBytes + r * rows_per_box * 128, map, h * 64, sg.hkv, s0, done);
             }
             __syncwarp();
           }
@@ -370,7 +480,7 @@ __global__ void __launch_bounds__(384, 1)
           dts::report(a.err, DTS_DEV_TIMEOUT);
           // give the copies already in flight a bounded chance to land
           for (int u = max(0, use - kSlots); u < use; ++u)
-            mbar_wait(&full[u % kSlots], static_cast<uint32_t>(u / kSlots) & 1u, abort_flag);
+            mbar_wait((u & 1) ? &vfull[u % kSlots] : &kfull[u % kSlots], kind_phase<kSlots>(u), abort_flag);
         }
       }
       __syncwarp();
@@ -379,7 +489,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
       constexpr uint32_t kIdescO = idesc_bf16(128, D, true);
       auto slot_of = [](int use) { return use % kSlots; };
-      auto phase_of = [](int use) { return static_cast<uint32_t>(use / kSlots) & 1u; };
+      auto kind_phase_of = [](int use) { return kind_phase<kSlots>(use); };
       // One thread issues every MMA, so the issue loop must stay short: the
       // descriptors are built once and only their 16-byte start-address field
       // (bits 0-13) moves, by compile-time offsets, between MMAs.
@@ -414,7 +524,7 @@ __global__ void __launch_bounds__(384, 1)
         const int nt = sg.nt;
         // S for the segment's first tile needs its Q tiles and K
         ok = mbar_wait(q_full, static_cast<uint32_t>(segc) & 1u, abort_flag) &&
-             mbar_wait(&full[slot_of(use)], phase_of(use), abort_flag);
+             mbar_wait(&kfull[slot_of(use)], kind_phase_of(use), abort_flag);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -439,22 +549,9 @@ __global__ void __launch_bounds__(384, 1)
           const int vslot = slot_of(vuse);
           const int kuse = use + 2 * (j + 1);
           const bool more = j + 1 < nkt;
-          ok = mbar_wait(&full[vslot], phase_of(vuse), abort_flag) &&
-               (!more || mbar_wait(&full[slot_of(kuse)], phase_of(kuse), abort_flag));
+          ok = mbar_wait(&vready[vslot], kind_phase_of(vuse), abort_flag) &&
+               (!more || mbar_wait(&kfull[slot_of(kuse)], kind_phase_of(kuse), abort_flag));
           if (!ok) break;
-          const int nvalid = min(128, sg.P - (sg.lt0 + j) * 128);
-          if (nvalid < 128) {
-            // keys past the prefix's end: zero their V rows so that 0 * (stale or
-            // non-finite V) cannot reach O
-            uint8_t *vt = sKV + vslot * kTileBytes;
-            for (int h = 0; h < D / 64; ++h) {
-              uint4 *p = reinterpret_cast<uint4 *>(vt + h * S::kBlockBytes + nvalid * 128);
-              const int n16 = (128 - nvalid) * 8;
-              for (int e = lane; e < n16; e += 32) p[e] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async();
-            __syncwarp();
-          }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t >= nt) break;
@@ -496,6 +593,46 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) mma_commit(drain);
       __syncwarp();
       mbar_wait(drain, 0, abort_flag);
+    } else if (warp == 2) {
+      // ---------------------------------------------------------- V-tile warp
+      // Hands every V tile to the MMA warp (vready) once it has landed, after
+      // cleaning the ones that reach the window (clean_window_v), and
+      // publishes each segment's poisoned window keys (win_bar).
+      int use = 0, prev_nt = 0;
+      int scnt[2] = {0, 0};  // segments each softmax group has taken part in
+      bool ok = true;
+      while (ok && walker.next(a, sg)) {
+        const int nkt = sg.lt1 - sg.lt0;
+        uint64_t seg_poison = 0;
+        for (int j = 0; j < nkt && ok; ++j) {
+          const int vuse = use + 2 * j + 1;
+          const int vslot = vuse % kSlots;
+          ok = mbar_wait(&vfull[vslot], kind_phase<kSlots>(vuse), abort_flag);
+          if (!ok) break;
+          const int kbase = (sg.lt0 + j) * 128;
+          if (kbase + 128 > sg.P)  // the window's tiles (and the unit's end)
+            seg_poison |= clean_window_v<D>(sKV + vslot * kTileBytes, kbase - sg.P, a.N, lane);
+          if (lane == 0) mbar_arrive(&vready[vslot]);
+          __syncwarp();
+        }
+        // The groups that read the previous segment's mask must be past it
+        // (o_free follows their read) before it is overwritten.
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ok && t < prev_nt && scnt[t] > 0)
+            ok = mbar_wait(&o_free[t], static_cast<uint32_t>(scnt[t] - 1) & 1u, abort_flag);
+        prev_nt = sg.nt;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (t < sg.nt) ++scnt[t];
+        if (lane == 0) {
+          *poison = seg_poison;
+          mbar_arrive(win_bar);
+        }
+        __syncwarp();
+        use += 2 * nkt;
+      }
+      if (!ok) dts::report(a.err, DTS_DEV_TIMEOUT);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n" ::: "memory");
@@ -506,16 +643,27 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
     const float c = a.scale_log2;
-    int tcnt = 0, scnt = 0;
+    const uint64_t node_bits = a.N < 64 ? (1ull << a.N) - 1ull : ~0ull;
+    int tcnt = 0, scnt = 0, wcnt = 0;
     bool ok = true;
     while (ok && walker.next(a, sg)) {
+      const uint32_t wpar = static_cast<uint32_t>(wcnt++) & 1u;  // win_bar completes once per segment
+      const bool whole = sg.lt0 == 0 && sg.lt1 == sg.nkt;        // the unit lies inside this segment
       if (t >= sg.nt) continue;
       const int nkt = sg.lt1 - sg.lt0;
       const int prow = t * a.rt + r;                      // row within the unit's slot
       const int R = sg.pair * 2 * a.rt + prow;            // row of the KV head
       const bool warp_valid = wq * 32 < a.rt && sg.pair * 2 * a.rt + t * a.rt + wq * 32 < a.M;
+      const bool valid = warp_valid && r < a.rt && R < a.M;
+      // the row's ancestor mask (bits >= N clear), read where a tile reaches the window
+      auto row_mask = [&]() -> uint64_t {
+        return valid ? (a.mask[static_cast<int64_t>(sg.b) * a.N + R / a.g] & node_bits) : 0ull;
+      };
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nkt; ++j) {
+        const bool in_window = (sg.lt0 + j) * 128 + 128 > sg.P;
+        uint64_t mrow = 0;
+        if (in_window) mrow = row_mask();  // in flight during the wait below
         if (!mbar_wait(&s_full[t], static_cast<uint32_t>(tcnt + j) & 1u, abort_flag)) {
           ok = false;
           break;
@@ -526,13 +674,16 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sv[q]);
           tmem_wait_ld();
-          const int nvalid = min(128, sg.P - (sg.lt0 + j) * 128);
-          if (nvalid < 128) {  // the prefix's last tile: keys past its end score -inf
+          const int kbase = (sg.lt0 + j) * 128;
+          if (in_window) {
+            // the window's tiles: a key counts only if the row may see it
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t vis = visible_word(kbase + q * 32 - sg.P, mrow);
 #pragma unroll
               for (int k = 0; k < 32; ++k)
-                if (q * 32 + k >= nvalid) sv[q][k] = __float_as_uint(-INFINITY);
+                if (!(vis & (1u << k))) sv[q][k] = __float_as_uint(-INFINITY);
+            }
           }
           float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -547,12 +698,15 @@ __global__ void __launch_bounds__(384, 1)
           const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
           float m_use = m_run;
           if (m_new > m_run + 8.f) m_use = m_new;  // lazy rescale: P stays below 2^8
-          const float alpha = ex2(m_run - m_use);
+          // a row may see no key of a tile (or of a whole segment): m_use stays
+          // -inf, P is 0 and nothing rescales
+          const float m_sub = m_use == -INFINITY ? 0.f : m_use;
+          const float alpha = m_use == -INFINITY ? 1.f : ex2(m_run - m_use);
           // P = 2^(s*c - m_use) as bf16 pairs, packed in place over the consumed
           // S registers: pair (q, k) lands in sv[q >> 1][(q & 1) * 16 + k / 2],
           // an entry already read. The scale-and-shift runs two lanes per FMA.
           const uint64_t cc = f2_pack(c, c);
-          const uint64_t nm = f2_pack(-m_use, -m_use);
+          const uint64_t nm = f2_pack(-m_sub, -m_sub);
           uint64_t sum0 = f2_pack(0.f, 0.f), sum1 = sum0;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -598,34 +752,75 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(&p_full[t]);
       }
-      if (!ok || !mbar_wait(&o_fin[t], static_cast<uint32_t>(scnt) & 1u, abort_flag)) {
+      if (!ok || !mbar_wait(&o_fin[t], static_cast<uint32_t>(scnt) & 1u, abort_flag) ||
+          !mbar_wait(win_bar, wpar, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (warp_valid) {
-        const bool valid = r < a.rt && R < a.M;
-        const int64_t slot_row = (static_cast<int64_t>(sg.unit) + blockIdx.x) * a.slot_rows + prow;
-        const float inv_l = 1.f / l_run;
-        float *dst = a.o_part + slot_row * D;
+      // a row that sees a window key whose V row was not finite reads NaN
+      const uint64_t seg_poison = *poison;
+      const bool poisoned = seg_poison != 0ull && (row_mask() & seg_poison) != 0ull;
+      const int node = R / a.g;  // the row's tree node
+      const int64_t node_row = static_cast<int64_t>(sg.b) * a.N + node;
+      // l_run = 0: the row saw no key here (the part drops out of the merge);
+      // a non-finite l_run (a non-finite score) stays non-finite
+      const float inv_l = l_run == 0.f ? 0.f : 1.f / l_run;
+      const float lse_row = l_run == 0.f ? -INFINITY : m_run + __log2f(l_run);
+      const int h = sg.hkv * a.g + (R - node * a.g);
+      const int64_t out_row = node_row * a.Hq + h;
+      if (whole) {
+        // ---- the whole unit is in this segment: write the rows
+        if (warp_valid) {
 #pragma unroll 1
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t ov[32];
-          tmem_ld32(tO + q * 32, ov);
-          tmem_wait_ld();
-          if (valid) {
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(tO + q * 32, ov);
+            tmem_wait_ld();
+            if (valid) {
+              uint4 *dst = reinterpret_cast<uint4 *>(a.out + out_row * D + q * 32);
 #pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-              float4 v = make_float4(__uint_as_float(ov[k]) * inv_l, __uint_as_float(ov[k + 1]) * inv_l,
-                                     __uint_as_float(ov[k + 2]) * inv_l, __uint_as_float(ov[k + 3]) * inv_l);
-              *reinterpret_cast<float4 *>(dst + q * 32 + k) = v;
+              for (int k = 0; k < 32; k += 8) {
+                uint4 v;
+                v.x = dts::pack_bf16x2(__uint_as_float(ov[k]) * inv_l, __uint_as_float(ov[k + 1]) * inv_l);
+                v.y = dts::pack_bf16x2(__uint_as_float(ov[k + 2]) * inv_l, __uint_as_float(ov[k + 3]) * inv_l);
+                v.z = dts::pack_bf16x2(__uint_as_float(ov[k + 4]) * inv_l, __uint_as_float(ov[k + 5]) * inv_l);
+                v.w = dts::pack_bf16x2(__uint_as_float(ov[k + 6]) * inv_l, __uint_as_float(ov[k + 7]) * inv_l);
+                if (poisoned) v = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+                dst[k / 8] = v;
+              }
             }
           }
+          if (valid) a.lse2[out_row] = lse_row;
         }
-        if (valid) a.lse_part[slot_row] = m_run + __log2f(l_run);
+        tc_fence_before();
+        mbar_arrive(&o_free[t]);
+      } else {
+        // ---- one of several segments: write the partial (the merge pass
+        // combines the unit's partials)
+        const int64_t slot_row = (static_cast<int64_t>(sg.unit) + blockIdx.x) * a.slot_rows + prow;
+        if (warp_valid) {
+          float *dst = a.o_part + slot_row * D;
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(tO + q * 32, ov);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int k = 0; k < 32; k += 4) {
+                float4 v = make_float4(__uint_as_float(ov[k]) * inv_l, __uint_as_float(ov[k + 1]) * inv_l,
+                                       __uint_as_float(ov[k + 2]) * inv_l, __uint_as_float(ov[k + 3]) * inv_l);
+                if (poisoned) v = make_float4(NAN, NAN, NAN, NAN);
+                *reinterpret_cast<float4 *>(dst + q * 32 + k) = v;
+              }
+            }
+          }
+          if (valid) a.lse_part[slot_row] = lse_row;
+        }
+        tc_fence_before();
+        mbar_arrive(&o_free[t]);
       }
-      tc_fence_before();
-      mbar_arrive(&o_free[t]);
       tcnt += nkt;
       ++scnt;
     }
@@ -640,219 +835,129 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ============================================================================
-// window + merge pass
+// merge pass
 // ============================================================================
-struct WindowArgs {
-  const uint16_t *q;  // rotated queries (bf16)
-  const uint16_t *k_cache;
-  const uint16_t *v_cache;
-  const int32_t *page_table;
-  const int32_t *prefix_len;
-  const uint64_t *mask;
+struct MergeArgs {
   const float *o_part;
   const float *lse_part;
   const int64_t *tiles_before;
+  const int32_t *prefix_len;
   uint16_t *out;
   float *lse2;
-  int32_t *err;
-  int64_t num_slots, max_prefix;
-  int B, N, Hq, Hkv, g, rt, n_pairs, slot_rows, heads_per_warp, max_pages, page_shift, grid, has_prefix;
-  float scale_log2;
+  int64_t max_prefix, capacity;
+  int B, N, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;
 };
 
-// Lane l holds elements {2l, 2l+1, D/2+2l, D/2+2l+1} (D = 128) or {l, D/2+l} (D = 64).
+// One warp per 8 consecutive rows of a unit's slot (lane l holds columns
+// [E l, E l + E), E = d/32). A unit whose key tiles all fell to one CTA was
+// written by the tree pass; the others merge their parts' partial rows by
+// their LSEs: O = sum_k 2^(lse_k - m) O_k / sum_k 2^(lse_k - m),
+// lse = m + log2(sum_k 2^(lse_k - m)), m the largest lse_k.
 template <int D>
-__device__ __forceinline__ void load_row(const uint16_t *row, int lane, float (&x)[D / 32]) {
-  if constexpr (D == 128) {
-    const uint32_t w1 = reinterpret_cast<const uint32_t *>(row)[lane];
-    const uint32_t w2 = reinterpret_cast<const uint32_t *>(row + 64)[lane];
-    x[0] = dts::bf16_lo(w1);
-    x[1] = dts::bf16_hi(w1);
-    x[2] = dts::bf16_lo(w2);
-    x[3] = dts::bf16_hi(w2);
-  } else {
-    x[0] = __uint_as_float(static_cast<uint32_t>(row[lane]) << 16);
-    x[1] = __uint_as_float(static_cast<uint32_t>(row[32 + lane]) << 16);
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-template <int D, int HW>
-__global__ void __launch_bounds__(256) tree_window_kernel(const __grid_constant__ WindowArgs a) {
+__global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__ MergeArgs a) {
+  constexpr int kRows = 8;
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
-  int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int groups = a.g / HW;
-  const int64_t total = static_cast<int64_t>(a.B) * a.N * a.Hkv * groups;
-  if (wid >= total) return;
-  const int hg = static_cast<int>(wid % groups);
-  wid /= groups;
-  const int hkv = static_cast<int>(wid % a.Hkv);
-  const int64_t node = wid / a.Hkv;  // b * N + i
-  const int b = static_cast<int>(node / a.N);
-  const int i = static_cast<int>(node - static_cast<int64_t>(b) * a.N);
-  const int h0 = hkv * a.g + hg * HW;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int blocks_per_unit = (a.slot_rows + kRows - 1) / kRows;
+  const int64_t unit = wid / blocks_per_unit;
+  const int per_req = a.Hkv * a.n_pairs;
+  if (unit >= static_cast<int64_t>(a.B) * per_req) return;
+  const int rb = static_cast<int>(wid - unit * blocks_per_unit);
+  const int b = static_cast<int>(unit / per_req);
+  const int uir = static_cast<int>(unit - static_cast<int64_t>(b) * per_req);
+  const int hkv = uir / a.n_pairs, pair = uir - hkv * a.n_pairs;
   const int P = a.prefix_len[b];
+  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.N > a.capacity) return;  // NaN rows from prep
+  const int nkt = (P + a.N + 127) >> 7;
+  const int64_t T = a.tiles_before[a.B], G = a.grid;
+  const int64_t start = a.tiles_before[b] + static_cast<int64_t>(uir) * nkt;
+  const int64_t c_first = ((start + 1) * G - 1) / T, c_last = ((start + nkt) * G - 1) / T;
+  if (c_first == c_last) return;  // one part: the tree pass wrote these rows
+  auto owns = [&](int64_t c) { return c * T / G < (c + 1) * T / G; };
 
-  if (P < 0 || P > a.max_prefix ||
-      static_cast<int64_t>(P) + a.N > (static_cast<int64_t>(a.max_pages) << a.page_shift)) {
-    if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
-    for (int u = 0; u < HW; ++u) {
-      uint16_t *o = a.out + (node * a.Hq + h0 + u) * D;
-      for (int e = lane; e < D; e += 32) o[e] = 0x7FC0;  // NaN
-      if (lane == 0) a.lse2[node * a.Hq + h0 + u] = __int_as_float(0x7FC00000);
-    }
-    return;
+  // lane = (part k of a pass of four) * 8 + row i: the LSE it reads
+  const int i_row = lane & 7;
+  const int prow_l = rb * kRows + i_row;
+  const bool row_ok = prow_l < a.slot_rows;
+  float mx = -INFINITY;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    const int64_t c = c0 + (lane >> 3);
+    if (c <= c_last && row_ok && owns(c)) mx = fmaxf(mx, a.lse_part[(unit + c) * a.slot_rows + prow_l]);
   }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
 
-  float q[HW][E];
+  float acc[kRows][E];
 #pragma unroll
-  for (int u = 0; u < HW; ++u) load_row<D>(a.q + (node * a.Hq + h0 + u) * D, lane, q[u]);
-
-  float m[HW], l[HW], acc[HW][E];
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
-  for (int u = 0; u < HW; ++u) {
-    m[u] = -INFINITY;
-    l[u] = 0.f;
+    for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
+  float den = 0.f;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    const int64_t c = c0 + (lane >> 3);
+    float lse = -INFINITY;
+    if (c <= c_last && row_ok && owns(c)) lse = a.lse_part[(unit + c) * a.slot_rows + prow_l];
+    const float w = lse == -INFINITY ? 0.f : dts::ptx::ex2(lse - mx);  // a part that saw no key drops out
+    den += w;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[u][e] = 0.f;
-  }
-
-  // prefix segments of this row's unit: the CTAs that own the unit's first and
-  // last key tile, and every one between, each left one partial in slot
-  // (unit + CTA index). Largest LSE first, then an order-free weighted sum.
-  const int nkt = a.has_prefix ? (P + 127) >> 7 : 0;
-  if (nkt > 0) {
-    const int64_t T = a.tiles_before[a.B];
-    const int R = i * a.g + hg * HW;  // all HW heads share the pair
-    const int pair = R / (2 * a.rt);
-    const int prow0 = R - pair * 2 * a.rt;
-    const int uir = hkv * a.n_pairs + pair;
-    const int64_t unit = static_cast<int64_t>(b) * a.Hkv * a.n_pairs + uir;
-    const int64_t start = a.tiles_before[b] + static_cast<int64_t>(uir) * nkt;
-    const int64_t G = a.grid;
-    const int64_t c_first = ((start + 1) * G - 1) / T;
-    const int64_t c_last = ((start + nkt) * G - 1) / T;
-    // with fewer tiles than CTAs some CTAs own no tile (and wrote no partial)
-    auto owns_tiles = [&](int64_t cc) { return cc * T / G < (cc + 1) * T / G; };
-    for (int64_t cc = c_first; cc <= c_last; ++cc) {
-      if (!owns_tiles(cc)) continue;
-      const int64_t base = (unit + cc) * a.slot_rows + prow0;
+    for (int k = 0; k < 4; ++k) {
+      const int64_t ck = c0 + k;
+      if (ck > c_last) break;
+      if (!owns(ck)) continue;
+      const float *base = a.o_part + ((unit + ck) * a.slot_rows + rb * kRows) * D + E * lane;
+      float x[kRows][E];
 #pragma unroll
-      for (int u = 0; u < HW; ++u) m[u] = fmaxf(m[u], a.lse_part[base + u]);
-    }
-#pragma unroll 2
-    for (int64_t cc = c_first; cc <= c_last; ++cc) {
-      if (!owns_tiles(cc)) continue;
-      const int64_t base = (unit + cc) * a.slot_rows + prow0;
-#pragma unroll
-      for (int u = 0; u < HW; ++u) {
-        const float wgt = dts::ptx::ex2(a.lse_part[base + u] - m[u]);
-        const float *op = a.o_part + (base + u) * D;
-        float x[E];
-        if constexpr (D == 128) {
-          const float2 lo2 = reinterpret_cast<const float2 *>(op)[lane];
-          const float2 hi2 = reinterpret_cast<const float2 *>(op + 64)[lane];
-          x[0] = lo2.x;
-          x[1] = lo2.y;
-          x[2] = hi2.x;
-          x[3] = hi2.y;
+      for (int i = 0; i < kRows; ++i) {
+        if (rb * kRows + i < a.slot_rows) {
+          if constexpr (E == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(base + i * D);
+            x[i][0] = v.x;
+            x[i][1] = v.y;
+            x[i][2] = v.z;
+            x[i][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2 *>(base + i * D);
+            x[i][0] = v.x;
+            x[i][1] = v.y;
+          }
         } else {
-          x[0] = op[lane];
-          x[1] = op[32 + lane];
-        }
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[u][e] = fmaf(x[e], wgt, acc[u][e]);
-        l[u] += wgt;
+          for (int e = 0; e < E; ++e) x[i][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, k * 8 + i);
+        if (wi == 0.f) continue;  // warp-uniform
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[i][e] = fmaf(x[i][e], wi, acc[i][e]);
       }
     }
   }
-
-  // window: the node's ancestors (and itself), in ascending node index
-  const int ps = 1 << a.page_shift;
-  uint64_t mk = a.mask[node];
-  if (a.N < 64) mk &= (1ull << a.N) - 1;
-  const int64_t pt_row = static_cast<int64_t>(b) * a.max_pages;
-  // Ancestors go four at a time: their K/V rows are all in flight together,
-  // and the four dot products of each head reduce across the warp side by side.
-  constexpr int kBatch = 4;
-  while (mk) {
-    float kx[kBatch][E], vx[kBatch][E];
-    bool have[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      have[k] = false;
-      if (mk) {
-        const int j = __ffsll(static_cast<long long>(mk)) - 1;
-        mk &= mk - 1;
-        const int64_t logical = static_cast<int64_t>(P) + j;
-        const int pid = a.page_table[pt_row + (logical >> a.page_shift)];
-        const int64_t slot = static_cast<int64_t>(pid) * ps + (logical & (ps - 1));
-        if (pid < 0 || slot >= a.num_slots) {
-          if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
-        } else {
-          load_row<D>(a.k_cache + (slot * a.Hkv + hkv) * D, lane, kx[k]);
-          load_row<D>(a.v_cache + (slot * a.Hkv + hkv) * D, lane, vx[k]);
-          have[k] = true;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < HW; ++u) {
-      float s[kBatch];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        float d = 0.f;
-        if (have[k]) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) d = fmaf(q[u][e], kx[k][e], d);
-        }
-        s[k] = d;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], o);
-      float mn = m[u];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        s[k] *= a.scale_log2;
-        if (have[k]) mn = fmaxf(mn, s[k]);
-      }
-      const float sa = mn == -INFINITY ? 1.f : dts::ptx::ex2(m[u] - mn);  // -inf: nothing seen yet
-      l[u] *= sa;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[u][e] *= sa;
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        if (!have[k]) continue;
-        const float w = dts::ptx::ex2(s[k] - mn);
-        l[u] += w;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[u][e] = fmaf(vx[k][e], w, acc[u][e]);
-      }
-      m[u] = mn;
-    }
-  }
+  den += __shfl_xor_sync(0xffffffffu, den, 8);
+  den += __shfl_xor_sync(0xffffffffu, den, 16);
 
 #pragma unroll
-  for (int u = 0; u < HW; ++u) {
-    const float inv = l[u] > 0.f ? 1.f / l[u] : 0.f;
-    uint16_t *o = a.out + (node * a.Hq + h0 + u) * D;
-    if constexpr (D == 128) {
-      reinterpret_cast<uint32_t *>(o)[lane] = dts::pack_bf16x2(acc[u][0] * inv, acc[u][1] * inv);
-      reinterpret_cast<uint32_t *>(o + 64)[lane] = dts::pack_bf16x2(acc[u][2] * inv, acc[u][3] * inv);
+  for (int i = 0; i < kRows; ++i) {
+    const int prow = rb * kRows + i;
+    const float den_i = __shfl_sync(0xffffffffu, den, i);
+    const float mx_i = __shfl_sync(0xffffffffu, mx, i);
+    const int R = pair * 2 * a.rt + prow;  // row of the KV head
+    if (prow >= a.slot_rows || R >= a.M) continue;
+    const int node = R / a.g;
+    const int64_t out_row = (static_cast<int64_t>(b) * a.N + node) * a.Hq + hkv * a.g + (R - node * a.g);
+    const float inv = den_i == 0.f ? 0.f : 1.f / den_i;  // (a NaN sum stays NaN)
+    if constexpr (E == 4) {
+      uint2 v;
+      v.x = dts::pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
+      v.y = dts::pack_bf16x2(acc[i][2] * inv, acc[i][3] * inv);
+      *reinterpret_cast<uint2 *>(a.out + out_row * D + E * lane) = v;
     } else {
-      const uint32_t w = dts::pack_bf16x2(acc[u][0] * inv, acc[u][1] * inv);
-      o[lane] = static_cast<uint16_t>(w & 0xFFFFu);
-      o[32 + lane] = static_cast<uint16_t>(w >> 16);
+      *reinterpret_cast<uint32_t *>(a.out + out_row * D + E * lane) =
+          dts::pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
     }
-    if (lane == 0) a.lse2[node * a.Hq + h0 + u] = l[u] > 0.f ? m[u] + __log2f(l[u]) : -INFINITY;
+    if (lane == 0) a.lse2[out_row] = den_i == 0.f ? -INFINITY : mx_i + __log2f(den_i);
   }
 }
 
@@ -918,19 +1023,6 @@ int launch_prefix(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMa
   return dts_host::launch_status();
 }
 
-template <int D>
-int launch_window(const WindowArgs &a, cudaStream_t s) {
-  const int64_t warps = static_cast<int64_t>(a.B) * a.N * a.Hkv * (a.g / a.heads_per_warp);
-  const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  switch (a.heads_per_warp) {
-    case 1: tree_window_kernel<D, 1><<<blocks, 256, 0, s>>>(a); break;
-    case 2: tree_window_kernel<D, 2><<<blocks, 256, 0, s>>>(a); break;
-    case 4: tree_window_kernel<D, 4><<<blocks, 256, 0, s>>>(a); break;
-    default: tree_window_kernel<D, 8><<<blocks, 256, 0, s>>>(a); break;
-  }
-  return dts_host::launch_status();
-}
-
 }  // namespace
 
 extern "C" size_t dts_tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d, int64_t max_prefix) {
@@ -974,93 +1066,92 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   const int page_shift = __builtin_ctz(static_cast<unsigned>(page_size));
   const int g = Hq / Hkv;
 
-  // 0. queries in the model dtype, rotated once
-  const uint16_t *q_eff = q;
-  if (positions != nullptr) {
-    RopeQArgs ra;
+  // 0. prep: rotated queries, NaN rows for bad prefix lengths
+  {
+    PrepArgs ra;
     ra.q = q;
     ra.positions = positions;
+    ra.prefix_len = prefix_len;
     ra.q_rot = q_rot;
+    ra.out = out;
+    ra.lse2 = lse2;
+    ra.err = err_dev;
+    ra.max_prefix = max_prefix;
+    ra.capacity = static_cast<int64_t>(max_pages) << page_shift;
     ra.rows = B * N;
+    ra.N = N;
     ra.Hq = Hq;
     ra.heads_per_thread = (Hq % 4 == 0) ? 4 : (Hq % 2 == 0) ? 2 : 1;
-    dts_host::make_rope_freqs(rope_theta, d, &ra.freqs);
+    if (positions != nullptr) dts_host::make_rope_freqs(rope_theta, d, &ra.freqs);
     const int64_t items = static_cast<int64_t>(B) * N * (Hq / ra.heads_per_thread) * (d / 16);
     const int blocks = static_cast<int>((items + 255) / 256);
-    if (d == 128) rope_q_kernel<128><<<blocks, 256, 0, s>>>(ra);
-    else rope_q_kernel<64><<<blocks, 256, 0, s>>>(ra);
+    if (d == 128) attn_prep_kernel<128><<<blocks, 256, 0, s>>>(ra);
+    else attn_prep_kernel<64><<<blocks, 256, 0, s>>>(ra);
     if (dts_host::launch_status() != DTS_OK) return DTS_ERR_CUDA;
-    q_eff = q_rot;
   }
+  const uint16_t *q_eff = positions != nullptr ? q_rot : q;
 
-  // 1. prefix pass, one CTA per SM
-  int grid = 0;
-  if (max_prefix > 0) {
-    const int sms = dts_host::sm_count();
-    grid = sms > 0 ? (sms < kMaxGrid ? sms : kMaxGrid) : 1;
-    CUtensorMap tk, tv, tq;
-    const int rpb = page_size < 128 ? page_size : 128;
-    if (!make_cache_map(&tk, k_cache, d, Hkv, num_slots, rpb) || !make_cache_map(&tv, v_cache, d, Hkv, num_slots, rpb) ||
-        !make_q_map(&tq, q_eff, d, g, Hkv, static_cast<int64_t>(B) * N, plan.npt))
-      return DTS_ERR_CUDA;
-    PrefixArgs pa;
-    pa.page_table = page_table;
-    pa.prefix_len = prefix_len;
-    pa.o_part = o_part;
-    pa.lse_part = lse_part;
-    pa.tiles_before = tiles_before;
-    pa.err = err_dev;
-    pa.num_slots = num_slots;
-    pa.max_prefix = max_prefix;
-    pa.B = B;
-    pa.N = N;
-    pa.Hq = Hq;
-    pa.Hkv = Hkv;
-    pa.g = g;
-    pa.M = N * g;
-    pa.rt = plan.rt;
-    pa.npt = plan.npt;
-    pa.n_pairs = plan.n_pairs;
-    pa.slot_rows = plan.slot_rows;
-    pa.max_pages = max_pages;
-    pa.page_shift = page_shift;
-    pa.scale_log2 = scale * kLog2e;
-    const int st = d == 128 ? launch_prefix<128>(tk, tv, tq, pa, grid, s) : launch_prefix<64>(tk, tv, tq, pa, grid, s);
-    if (st != DTS_OK) return st;
-  }
+  // 1. tree attention, one CTA per SM
+  const int sms = dts_host::sm_count();
+  const int grid = sms > 0 ? (sms < kMaxGrid ? sms : kMaxGrid) : 1;
+  CUtensorMap tk, tv, tq;
+  const int rpb = page_size < 128 ? page_size : 128;
+  if (!make_cache_map(&tk, k_cache, d, Hkv, num_slots, rpb) || !make_cache_map(&tv, v_cache, d, Hkv, num_slots, rpb) ||
+      !make_q_map(&tq, q_eff, d, g, Hkv, static_cast<int64_t>(B) * N, plan.npt))
+    return DTS_ERR_CUDA;
+  PrefixArgs pa;
+  pa.page_table = page_table;
+  pa.prefix_len = prefix_len;
+  pa.mask = mask;
+  pa.o_part = o_part;
+  pa.lse_part = lse_part;
+  pa.tiles_before = tiles_before;
+  pa.out = out;
+  pa.lse2 = lse2;
+  pa.err = err_dev;
+  pa.num_slots = num_slots;
+  pa.max_prefix = max_prefix;
+  pa.B = B;
+  pa.N = N;
+  pa.Hq = Hq;
+  pa.Hkv = Hkv;
+  pa.g = g;
+  pa.M = N * g;
+  pa.rt = plan.rt;
+  pa.npt = plan.npt;
+  pa.n_pairs = plan.n_pairs;
+  pa.slot_rows = plan.slot_rows;
+  pa.max_pages = max_pages;
+  pa.page_shift = page_shift;
+  pa.scale_log2 = scale * kLog2e;
+  const int st = d == 128 ? launch_prefix<128>(tk, tv, tq, pa, grid, s) : launch_prefix<64>(tk, tv, tq, pa, grid, s);
+  if (st != DTS_OK) return st;
 
-  // 2. window + merge pass
-  WindowArgs wa;
-  wa.q = q_eff;
-  wa.k_cache = k_cache;
-  wa.v_cache = v_cache;
-  wa.page_table = page_table;
-  wa.prefix_len = prefix_len;
-  wa.mask = mask;
-  wa.o_part = o_part;
-  wa.lse_part = lse_part;
-  wa.tiles_before = tiles_before;
-  wa.out = out;
-  wa.lse2 = lse2;
-  wa.err = err_dev;
-  wa.num_slots = num_slots;
-  wa.max_prefix = max_prefix;
-  wa.B = B;
-  wa.N = N;
-  wa.Hq = Hq;
-  wa.Hkv = Hkv;
-  wa.g = g;
-  wa.rt = plan.rt;
-  wa.n_pairs = plan.n_pairs;
-  wa.slot_rows = plan.slot_rows;
-  // at most 4 heads per warp: more warps in flight beat re-reading a few window rows
-  wa.heads_per_warp = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
-  wa.max_pages = max_pages;
-  wa.page_shift = page_shift;
-  wa.grid = grid;
-  wa.has_prefix = grid > 0 ? 1 : 0;
-  wa.scale_log2 = scale * kLog2e;
-  return d == 128 ? launch_window<128>(wa, s) : launch_window<64>(wa, s);
+  // 2. merge pass: units whose key tiles went to more than one CTA
+  MergeArgs ma;
+  ma.o_part = o_part;
+  ma.lse_part = lse_part;
+  ma.tiles_before = tiles_before;
+  ma.prefix_len = prefix_len;
+  ma.out = out;
+  ma.lse2 = lse2;
+  ma.max_prefix = max_prefix;
+  ma.capacity = static_cast<int64_t>(max_pages) << page_shift;
+  ma.B = B;
+  ma.N = N;
+  ma.Hq = Hq;
+  ma.Hkv = Hkv;
+  ma.g = g;
+  ma.M = N * g;
+  ma.rt = plan.rt;
+  ma.n_pairs = plan.n_pairs;
+  ma.slot_rows = plan.slot_rows;
+  ma.grid = grid;
+  const int64_t warps = plan.units * ((plan.slot_rows + 7) / 8);
+  const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+  if (d == 128) tree_merge_kernel<128><<<blocks, 256, 0, s>>>(ma);
+  else tree_merge_kernel<64><<<blocks, 256, 0, s>>>(ma);
+  return dts_host::launch_status();
 }
 
 // ============================================================================
