@@ -1,9 +1,9 @@
 """Benchmark of one full target-verify step of draft-tree speculative decoding.
 
 A step is one pass of the whole hot path over one synthetic batch:
-build_tree_mask -> write_window_kv -> tree_verify_attention (prep pass +
-tree attention pass) -> verify_tree_greedy -> compact_window_rows ->
-compact_rows. Inputs are resident in HBM when the timed region starts; L2 is
+build_tree_mask -> write_window_kv -> tree_verify_attention (query
+rotation, tensor-core pass over prefix and window keys, merge) ->
+verify_tree_greedy -> compact_window_rows -> compact_rows. Inputs are resident in HBM when the timed region starts; L2 is
 flushed (512 MiB write) before every timed step, outside the step's events.
 
 Default workload: eagle2_p8192_n64 (B=32, Hq=32, Hkv=8, d=128, P=8192, N=64),
@@ -229,18 +229,23 @@ def oracle_sample(inp: synth.VerifyInputs, b: int, nodes):
     return len(nodes)
 
 
-def cpu_rows_per_s(inp, steps=1, nodes_per_step=8):
+def cpu_rows_per_s(inp, steps=1, nodes_per_step=8, min_seconds=0.0, max_steps=100000):
+    """The oracle over `steps` samples (or, with min_seconds, as many as fit in
+    that time, at most max_steps); each sample is `nodes_per_step` verify rows
+    of one request (requests in turn) plus that request's walk and compaction."""
     w = inp.w
     n_nodes = min(nodes_per_step, w.N)
     rows = 0
+    done = 0
     t0 = time.perf_counter()
-    for s in range(steps):
-        b = s % w.B
-        nodes = [(s * n_nodes + k) % w.N for k in range(n_nodes)]
+    while done < max_steps and (done < steps or time.perf_counter() - t0 < min_seconds):
+        b = done % w.B
+        nodes = [(done * n_nodes + k) % w.N for k in range(n_nodes)]
         rows += oracle_sample(inp, b, nodes)
+        done += 1
     dt = time.perf_counter() - t0
-    return rows / dt, dt, f"{n_nodes} verify rows (all heads) of one request per step, plus that request's walk " \
-                          f"and compaction; {steps} step(s)"
+    return rows / dt, dt, f"{n_nodes} verify rows (all heads) of one request per sample, plus that request's walk " \
+                          f"and compaction; {done} sample(s), {rows} rows, {dt:.1f} s"
 
 
 # ----------------------------------------------------------------------------
@@ -262,8 +267,8 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     names = ("mask", "window_kv", "attention", "walk", "compact")
     calls = (db.mask_step, db.window_kv_step, db.attention_step, db.walk_step, db.compact_step)
-    # mask, window kv, attention prep + tree attention, walk, kv compaction, row compaction
-    launches_per_step = 7
+    # mask, window kv, attention (prep, tree pass, merge), walk, kv compaction, row compaction
+    launches_per_step = 8
 
     def one_step(ev=None):
         for k, c in enumerate(calls):
@@ -305,7 +310,7 @@ def run_ours(args, rank, world, local_rank):
     rows_per_step = w.B * w.N
     value = whole_job_rows_per_s(rows_per_step, world, ms_per_step)
 
-    # roofline of the attention call (prep pass + tree attention pass)
+    # roofline of the attention call (prep, tree pass, merge)
     attn_ms = statistics.mean(per_call["attention"])
     bytes_, flops = attention_work(inp)
     hbm, tf_burst, tf_sus, src = load_peaks()
@@ -317,7 +322,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": flops / (attn_ms / 1e3) / 1e12, "peak": tf_sus, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(args.workload)
-    roof["kernel"] = "tree_verify_attention (attn_prep_kernel + tree_prefix_kernel)"
+    roof["kernel"] = "tree_verify_attention (attn_prep_kernel + tree_prefix_kernel + tree_merge_kernel)"
     roof["algorithmic_bytes"] = bytes_
     roof["algorithmic_flops"] = flops
     roof["peak_source"] = f"{src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})"
@@ -371,7 +376,8 @@ def run_ours(args, rank, world, local_rank):
     if clocks is not None:
         line["clocks"] = clocks
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, sample = cpu_rows_per_s(inp, steps=1, nodes_per_step=min(16, w.N))
+        # about 12 s of oracle work on the host cores
+        v, dt, sample = cpu_rows_per_s(inp, steps=1, nodes_per_step=min(16, w.N), min_seconds=12.0)
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle",
                                 "sample": sample, "seconds": dt}
     return line

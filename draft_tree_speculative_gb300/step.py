@@ -36,7 +36,7 @@ def bf16_tensor(bits: np.ndarray, device):
 class DeviceBatch:
     """Device-resident inputs, outputs and scratch of one verify step."""
 
-    KERNELS_PER_STEP = 7  # mask, window kv, prefix, window/merge, walk, KV compaction, row compaction
+    KERNELS_PER_STEP = 8  # mask, window kv, attention prep, tree attention, merge, walk, KV compaction, row compaction
 
     def __init__(self, inp: synth.VerifyInputs, device="cuda", fp8_layers: Optional[int] = None,
                  compact_attention_kv: bool = True):

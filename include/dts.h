@@ -164,11 +164,15 @@ size_t dts_tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d,
  *
  * Query head h reads KV head h / (Hq/Hkv). d in {64, 128}; Hq % Hkv == 0;
  * 1 <= N <= 64; page_size a power of two in [8, 4096]; cache and q base
- * addresses 16-byte aligned. Window keys that a row's mask does not select are
- * never read for that row (non-finite values there cannot leak). A row whose
- * mask is 0 and whose prefix is empty gets out = 0 and lse2 = -inf.
- * DTS_DEV_BAD_SLOT if prefix_len[b] < 0, > max_prefix, or the window runs past
- * max_pages * page_size, or a page id is outside the pool.
+ * addresses 16-byte aligned. Window keys that a row's mask does not select
+ * count for nothing in that row: a non-finite K or V row of a window key
+ * makes only the rows that see it non-finite, and slots past the window never
+ * reach any row. A row whose mask is 0 and whose prefix is empty gets out = 0
+ * and lse2 = -inf. A request whose prefix_len[b] is < 0, > max_prefix, or
+ * puts the window past max_pages * page_size gets NaN rows and
+ * DTS_DEV_BAD_SLOT; so does a page id outside the pool.
+ * Launches three kernels on `stream` (query rotation, the tensor-core pass
+ * over prefix and window keys, the merge of units split over CTAs).
  */
 int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache,
                               const uint16_t *v_cache, int64_t num_slots,
