@@ -102,6 +102,7 @@ struct PrepArgs {
 template <int D>
 __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ PrepArgs a) {
   constexpr int kChunks = D / 16;
+  constexpr int kMaxHeads = 4;
   const int hgroups = a.Hq / a.heads_per_thread;
   const int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (it >= static_cast<int64_t>(a.rows) * hgroups * kChunks) return;
@@ -109,7 +110,19 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
   const int hg = static_cast<int>((it / kChunks) % hgroups);
   const int64_t node = it / (static_cast<int64_t>(kChunks) * hgroups);
   const int64_t b = node / a.N;
+  // every load up front: prefix length, position and the group's query chunks
   const int P = a.prefix_len[b];
+  const int pos = a.positions != nullptr ? a.positions[node] : 0;
+  uint4 x1[kMaxHeads], x2[kMaxHeads];
+  if (a.positions != nullptr) {
+#pragma unroll
+    for (int hh = 0; hh < kMaxHeads; ++hh) {
+      if (hh >= a.heads_per_thread) break;
+      const int64_t off = (node * a.Hq + hg * a.heads_per_thread + hh) * D + 8 * c;
+      x1[hh] = *reinterpret_cast<const uint4 *>(a.q + off);
+      x2[hh] = *reinterpret_cast<const uint4 *>(a.q + off + D / 2);
+    }
+  }
   if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.N > a.capacity) {
     // the attention pass skips this request: its rows read NaN
     if (c == 0 && hg == 0 && node == b * a.N) dts::report(a.err, DTS_DEV_BAD_SLOT);
@@ -124,17 +137,14 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
     return;
   }
   if (a.positions == nullptr) return;
-  const int pos = a.positions[node];
   float sn[8], cs[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) dts::rope_sincos(pos, a.freqs.w[8 * c + e], &sn[e], &cs[e]);
-  for (int hh = 0; hh < a.heads_per_thread; ++hh) {
-    const int h = hg * a.heads_per_thread + hh;
-    const int64_t off = (node * a.Hq + h) * D + 8 * c;
-    uint4 x1 = *reinterpret_cast<const uint4 *>(a.q + off);
-    uint4 x2 = *reinterpret_cast<const uint4 *>(a.q + off + D / 2);
-    uint32_t *w1 = reinterpret_cast<uint32_t *>(&x1);
-    uint32_t *w2 = reinterpret_cast<uint32_t *>(&x2);
+#pragma unroll
+  for (int hh = 0; hh < kMaxHeads; ++hh) {
+    if (hh >= a.heads_per_thread) break;
+    uint32_t *w1 = reinterpret_cast<uint32_t *>(&x1[hh]);
+    uint32_t *w2 = reinterpret_cast<uint32_t *>(&x2[hh]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float u0 = dts::bf16_lo(w1[e]), u1 = dts::bf16_hi(w1[e]);
@@ -143,8 +153,9 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
       w1[e] = dts::pack_bf16x2(u0 * c0 - v0 * s0, u1 * c1 - v1 * s1);
       w2[e] = dts::pack_bf16x2(v0 * c0 + u0 * s0, v1 * c1 + u1 * s1);
     }
-    *reinterpret_cast<uint4 *>(a.q_rot + off) = x1;
-    *reinterpret_cast<uint4 *>(a.q_rot + off + D / 2) = x2;
+    const int64_t off = (node * a.Hq + hg * a.heads_per_thread + hh) * D + 8 * c;
+    *reinterpret_cast<uint4 *>(a.q_rot + off) = x1[hh];
+    *reinterpret_cast<uint4 *>(a.q_rot + off + D / 2) = x2[hh];
   }
 }
 
@@ -846,6 +857,25 @@ struct MergeArgs {
   float *lse2;
   int64_t max_prefix, capacity;
   int B, N, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;
+  int owners32;  // every (tile index + 1) * groups fits in 32 bits
+};
+
+// Which group's range holds flat tile x, and whether group c owns any tile:
+// the tree pass gives group c the tiles [c T / G, (c + 1) T / G).
+struct Owners {
+  int64_t T, G;
+  bool w32;
+  __device__ int64_t of(int64_t x) const {  // ((x + 1) G - 1) / T
+    if (w32) return (static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(G) - 1u) / static_cast<uint32_t>(T);
+    return ((x + 1) * G - 1) / T;
+  }
+  __device__ bool owns(int64_t c) const {
+    if (w32) {
+      const uint32_t t = static_cast<uint32_t>(T), g = static_cast<uint32_t>(G), c32 = static_cast<uint32_t>(c);
+      return c32 * t / g < (c32 + 1u) * t / g;
+    }
+    return c * T / G < (c + 1) * T / G;
+  }
 };
 
 // One warp per 8 consecutive rows of a unit's slot (lane l holds columns
@@ -853,41 +883,49 @@ struct MergeArgs {
 // written by the tree pass; the others merge their parts' partial rows by
 // their LSEs: O = sum_k 2^(lse_k - m) O_k / sum_k 2^(lse_k - m),
 // lse = m + log2(sum_k 2^(lse_k - m)), m the largest lse_k.
+// Parts go four at a time: lane = part * 8 + row reads one LSE and decides
+// once whether its group owns tiles; the row loads of the four parts follow.
 template <int D>
 __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__ MergeArgs a) {
   constexpr int kRows = 8;
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int blocks_per_unit = (a.slot_rows + kRows - 1) / kRows;
-  const int64_t unit = wid / blocks_per_unit;
-  const int per_req = a.Hkv * a.n_pairs;
-  if (unit >= static_cast<int64_t>(a.B) * per_req) return;
+  const uint32_t wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t blocks_per_unit = static_cast<uint32_t>((a.slot_rows + kRows - 1) / kRows);
+  const uint32_t unit = wid / blocks_per_unit;
+  const uint32_t per_req = static_cast<uint32_t>(a.Hkv * a.n_pairs);
+  if (unit >= static_cast<uint32_t>(a.B) * per_req) return;
   const int rb = static_cast<int>(wid - unit * blocks_per_unit);
   const int b = static_cast<int>(unit / per_req);
-  const int uir = static_cast<int>(unit - static_cast<int64_t>(b) * per_req);
+  const int uir = static_cast<int>(unit - static_cast<uint32_t>(b) * per_req);
   const int hkv = uir / a.n_pairs, pair = uir - hkv * a.n_pairs;
   const int P = a.prefix_len[b];
   if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.N > a.capacity) return;  // NaN rows from prep
   const int nkt = (P + a.N + 127) >> 7;
-  const int64_t T = a.tiles_before[a.B], G = a.grid;
+  const Owners own{a.tiles_before[a.B], a.grid, a.owners32 != 0};
   const int64_t start = a.tiles_before[b] + static_cast<int64_t>(uir) * nkt;
-  const int64_t c_first = ((start + 1) * G - 1) / T, c_last = ((start + nkt) * G - 1) / T;
+  const int64_t c_first = own.of(start), c_last = own.of(start + nkt - 1);
   if (c_first == c_last) return;  // one part: the tree pass wrote these rows
-  auto owns = [&](int64_t c) { return c * T / G < (c + 1) * T / G; };
 
-  // lane = (part k of a pass of four) * 8 + row i: the LSE it reads
   const int i_row = lane & 7;
   const int prow_l = rb * kRows + i_row;
   const bool row_ok = prow_l < a.slot_rows;
+  const int64_t row0 = static_cast<int64_t>(unit) * a.slot_rows + prow_l;  // this lane's row in slot `unit`
+
+  // pass 1: the largest LSE of each row (the first four parts' LSEs are kept)
+  float lse_first = -INFINITY;
   float mx = -INFINITY;
   for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
     const int64_t c = c0 + (lane >> 3);
-    if (c <= c_last && row_ok && owns(c)) mx = fmaxf(mx, a.lse_part[(unit + c) * a.slot_rows + prow_l]);
+    float lse = -INFINITY;
+    if (c <= c_last && row_ok && own.owns(c)) lse = a.lse_part[row0 + c * a.slot_rows];
+    if (c0 == c_first) lse_first = lse;
+    mx = fmaxf(mx, lse);
   }
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
 
+  // pass 2: weights, their sum and the weighted rows
   float acc[kRows][E];
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
@@ -896,16 +934,20 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   float den = 0.f;
   for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
     const int64_t c = c0 + (lane >> 3);
-    float lse = -INFINITY;
-    if (c <= c_last && row_ok && owns(c)) lse = a.lse_part[(unit + c) * a.slot_rows + prow_l];
+    float lse = lse_first;
+    if (c0 != c_first) {
+      lse = -INFINITY;
+      if (c <= c_last && row_ok && own.owns(c)) lse = a.lse_part[row0 + c * a.slot_rows];
+    }
     const float w = lse == -INFINITY ? 0.f : dts::ptx::ex2(lse - mx);  // a part that saw no key drops out
     den += w;
+    // which of the four parts have rows to read (warp-uniform): a part whose
+    // weights are all 0 (not a group with tiles, or no key seen) is skipped
+    const uint32_t live = __ballot_sync(0xffffffffu, w != 0.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int64_t ck = c0 + k;
-      if (ck > c_last) break;
-      if (!owns(ck)) continue;
-      const float *base = a.o_part + ((unit + ck) * a.slot_rows + rb * kRows) * D + E * lane;
+      if (((live >> (8 * k)) & 0xFFu) == 0u) continue;
+      const float *base = a.o_part + ((static_cast<int64_t>(unit) + c0 + k) * a.slot_rows + rb * kRows) * D + E * lane;
       float x[kRows][E];
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
@@ -1147,6 +1189,11 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   ma.n_pairs = plan.n_pairs;
   ma.slot_rows = plan.slot_rows;
   ma.grid = grid;
+  {
+    // the largest possible tile total, times the groups, against 2^32
+    const int64_t max_tiles = static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + N + 127) / 128);
+    ma.owners32 = static_cast<double>(max_tiles + 1) * grid < 4294967296.0 ? 1 : 0;
+  }
   const int64_t warps = plan.units * ((plan.slot_rows + 7) / 8);
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   if (d == 128) tree_merge_kernel<128><<<blocks, 256, 0, s>>>(ma);
