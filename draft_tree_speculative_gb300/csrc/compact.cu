@@ -21,21 +21,37 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kPerThread = 8;  // words staged per thread per round
 
-// Validate one request's packed path. Fills dst/src with the moved rows (in
-// window-slot units) and returns their count, or -1 for a bad path.
-__device__ int collect_moves(const int32_t *__restrict__ path, int alen, int N, int *dst, int *src) {
-  if (alen < 1 || alen > N || path[0] != 0) return -1;
+// Validate one request's packed path with one warp (lane l looks at steps l
+// and l + 32; N <= 64). Fills dst/src with the moved rows (in window-slot
+// units, ascending) and returns their count in every lane, or -1 for a bad
+// path.
+__device__ int collect_moves_warp(const int32_t *__restrict__ path, int alen, int N, int *dst, int *src) {
+  const int lane = threadIdx.x & 31;
+  if (alen < 1 || alen > N) return -1;
   int n = 0;
-  for (int t = 1; t < alen; ++t) {
-    const int p = path[t];
-    if (p <= path[t - 1] || p >= N) return -1;
-    if (p != t) {
-      dst[n] = t;
-      src[n] = p;
-      ++n;
+  bool bad = false;
+  int prev_hi = 0;  // path[31], the predecessor of step 32
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int t = half * 32 + lane;
+    const int p = t < alen ? path[t] : 0;
+    int before = __shfl_up_sync(0xffffffffu, p, 1);
+    if (lane == 0) before = prev_hi;
+    prev_hi = __shfl_sync(0xffffffffu, p, 31);
+    if (t < alen) {
+      if (t == 0) bad |= p != 0;
+      else bad |= p <= before || p >= N;
     }
+    const bool moves = t >= 1 && t < alen && p != t;
+    const uint32_t m = __ballot_sync(0xffffffffu, moves);
+    if (moves) {
+      const int k = n + __popc(m & ((1u << lane) - 1u));
+      dst[k] = t;
+      src[k] = p;
+    }
+    n += __popc(m);
   }
-  return n;
+  return __any_sync(0xffffffffu, bad) ? -1 : n;
 }
 
 template <typename Word>
@@ -120,25 +136,28 @@ __global__ void __launch_bounds__(kThreads) compact_window_rows_kernel(
     if (threadIdx.x == 0 && (s_skip & 2) && b == 0) dts::report(err, DTS_DEV_BAD_BUFFER);
     return;
   }
-  if (threadIdx.x == 0) {
-    const int n = collect_moves(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
+  if (threadIdx.x < 32) {
+    const int n = collect_moves_warp(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
+    __syncwarp();
     if (n < 0) {
-      if (l == 0) dts::report(err, DTS_DEV_BAD_PATH);
-      s_n = 0;
+      if (threadIdx.x == 0) {
+        if (l == 0) dts::report(err, DTS_DEV_BAD_PATH);
+        s_n = 0;
+      }
     } else {
-      int ok = n;
-      for (int m = 0; m < n; ++m) {
+      bool bad = false;
+      for (int m = threadIdx.x; m < n; m += 32) {
         const int64_t d = wl[static_cast<int64_t>(b) * N + s_dst[m]];
         const int64_t s = wl[static_cast<int64_t>(b) * N + s_src[m]];
-        if (d < 0 || d >= e.num_slots || s < 0 || s >= e.num_slots) {
-          dts::report(err, DTS_DEV_BAD_SLOT);
-          ok = 0;
-          break;
-        }
+        bad |= d < 0 || d >= e.num_slots || s < 0 || s >= e.num_slots;
         s_dslot[m] = d;
         s_sslot[m] = s;
       }
-      s_n = ok;
+      bad = __any_sync(0xffffffffu, bad);
+      if (threadIdx.x == 0) {
+        if (bad) dts::report(err, DTS_DEV_BAD_SLOT);
+        s_n = bad ? 0 : n;
+      }
     }
   }
   __syncthreads();
@@ -158,14 +177,15 @@ __global__ void __launch_bounds__(kThreads) compact_rows_kernel(
   if (positions != nullptr)
     for (int i = threadIdx.x; i < N; i += kThreads) positions[static_cast<int64_t>(b) * N + i] = vc[b] + i;
   if (hidden == nullptr) return;
-  if (threadIdx.x == 0) {
-    const int n = collect_moves(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
-    if (n < 0) dts::report(err, DTS_DEV_BAD_PATH);
-    for (int m = 0; m < n; ++m) {
+  if (threadIdx.x < 32) {
+    const int n = collect_moves_warp(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
+    __syncwarp();
+    if (n < 0 && threadIdx.x == 0) dts::report(err, DTS_DEV_BAD_PATH);
+    for (int m = threadIdx.x; m < n; m += 32) {
       s_dslot[m] = static_cast<int64_t>(b) * N + s_dst[m];
       s_sslot[m] = static_cast<int64_t>(b) * N + s_src[m];
     }
-    s_n = n < 0 ? 0 : n;
+    if (threadIdx.x == 0) s_n = n < 0 ? 0 : n;
   }
   __syncthreads();
   if (s_n == 0) return;

@@ -2,7 +2,7 @@
 // and its value go to the slot of logical position prefix_len[b] + i.
 // [TS] "Position follows depth, slot follows node index".
 //
-// One warp per (node, KV head). Lane l holds the rotate-half pairs
+// One warp per node, all its KV heads. Lane l holds the rotate-half pairs
 // (2l, 2l+1 | d/2+2l, d/2+2l+1) for d = 128, or (l | d/2+l) for d = 64.
 #include "common.cuh"
 
@@ -23,58 +23,85 @@ struct WindowKvArgs {
   dts::RopeFreqs freqs;
 };
 
+// One warp per node: the RoPE angles depend on the node only, so they are
+// computed once and applied to all its KV heads; every head's K and V loads
+// are issued before the page-table lookup.
 template <int D>
 __global__ void __launch_bounds__(256) write_window_kv_kernel(const __grid_constant__ WindowKvArgs a) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int kMaxHeads = 16;  // heads held in registers per pass
+  const int node = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // b * N + i
   const int lane = threadIdx.x & 31;
-  const int total = a.B * a.N * a.Hkv;
-  if (warp >= total) return;
-  const int h = warp % a.Hkv;
-  const int node = warp / a.Hkv;  // b * N + i
+  if (node >= a.B * a.N) return;
   const int b = node / a.N;
   const int i = node - b * a.N;
   const int P = a.prefix_len[b];
+  const int pos = a.positions[node];
   const int ps = 1 << a.page_shift;
   const int64_t logical = static_cast<int64_t>(P) + i;
   const int64_t page = logical >> a.page_shift;
-  int64_t slot = -1;
-  if (P >= 0 && page < a.max_pages) {
-    const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + page];
-    const int64_t s = static_cast<int64_t>(pid) * ps + (logical & (ps - 1));
-    if (pid >= 0 && s < a.num_slots) slot = s;
-  }
-  if (slot < 0) {
-    if (lane == 0 && h == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
-    if (lane == 0 && h == 0 && a.write_locations) a.write_locations[node] = -1;
-    return;
-  }
-  if (lane == 0 && h == 0 && a.write_locations) a.write_locations[node] = slot;
-  const int pos = a.positions[node];
-  const uint16_t *kin = a.k_new + (static_cast<int64_t>(node) * a.Hkv + h) * D;
-  const uint16_t *vin = a.v_new + (static_cast<int64_t>(node) * a.Hkv + h) * D;
-  uint16_t *kout = a.k_cache + (slot * a.Hkv + h) * D;
-  uint16_t *vout = a.v_cache + (slot * a.Hkv + h) * D;
-  if constexpr (D == 128) {
-    const int k0 = 2 * lane;
-    const uint32_t x1 = reinterpret_cast<const uint32_t *>(kin)[lane];        // elems k0, k0+1
-    const uint32_t x2 = reinterpret_cast<const uint32_t *>(kin + 64)[lane];   // elems 64+k0, 64+k0+1
-    float s0, c0, s1, c1;
-    dts::rope_sincos(pos, a.freqs.w[k0], &s0, &c0);
-    dts::rope_sincos(pos, a.freqs.w[k0 + 1], &s1, &c1);
-    const float a0 = dts::bf16_lo(x1), a1 = dts::bf16_hi(x1);
-    const float b0 = dts::bf16_lo(x2), b1 = dts::bf16_hi(x2);
-    reinterpret_cast<uint32_t *>(kout)[lane] = dts::pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
-    reinterpret_cast<uint32_t *>(kout + 64)[lane] = dts::pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
-    reinterpret_cast<uint2 *>(vout)[lane] = reinterpret_cast<const uint2 *>(vin)[lane];
-  } else {
-    const float a0 = __uint_as_float(static_cast<uint32_t>(kin[lane]) << 16);
-    const float b0 = __uint_as_float(static_cast<uint32_t>(kin[32 + lane]) << 16);
-    float s0, c0;
-    dts::rope_sincos(pos, a.freqs.w[lane], &s0, &c0);
-    const uint32_t r = dts::pack_bf16x2(a0 * c0 - b0 * s0, b0 * c0 + a0 * s0);
-    kout[lane] = static_cast<uint16_t>(r & 0xFFFFu);
-    kout[32 + lane] = static_cast<uint16_t>(r >> 16);
-    reinterpret_cast<uint32_t *>(vout)[lane] = reinterpret_cast<const uint32_t *>(vin)[lane];
+  const bool page_ok = P >= 0 && page < a.max_pages;
+  const int pid = page_ok ? a.page_table[static_cast<int64_t>(b) * a.max_pages + page] : -1;
+  for (int h0 = 0; h0 < a.Hkv; h0 += kMaxHeads) {
+    const int nh = min(kMaxHeads, a.Hkv - h0);
+    uint32_t k1[kMaxHeads], k2[kMaxHeads];
+    uint2 v[kMaxHeads];
+#pragma unroll
+    for (int u = 0; u < kMaxHeads; ++u) {
+      if (u >= nh) break;
+      const uint16_t *kin = a.k_new + (static_cast<int64_t>(node) * a.Hkv + h0 + u) * D;
+      const uint16_t *vin = a.v_new + (static_cast<int64_t>(node) * a.Hkv + h0 + u) * D;
+      if constexpr (D == 128) {
+        k1[u] = reinterpret_cast<const uint32_t *>(kin)[lane];       // elems 2l, 2l+1
+        k2[u] = reinterpret_cast<const uint32_t *>(kin + 64)[lane];  // elems 64+2l, 64+2l+1
+        v[u] = reinterpret_cast<const uint2 *>(vin)[lane];
+      } else {
+        k1[u] = kin[lane];
+        k2[u] = kin[32 + lane];
+        v[u].x = reinterpret_cast<const uint32_t *>(vin)[lane];
+        v[u].y = 0;
+      }
+    }
+    const int64_t slot = static_cast<int64_t>(pid) * ps + (logical & (ps - 1));
+    if (pid < 0 || slot >= a.num_slots) {
+      if (lane == 0 && h0 == 0) {
+        dts::report(a.err, DTS_DEV_BAD_SLOT);
+        if (a.write_locations) a.write_locations[node] = -1;
+      }
+      return;
+    }
+    if (lane == 0 && h0 == 0 && a.write_locations) a.write_locations[node] = slot;
+    if constexpr (D == 128) {
+      const int k0 = 2 * lane;
+      float s0, c0, s1, c1;
+      dts::rope_sincos(pos, a.freqs.w[k0], &s0, &c0);
+      dts::rope_sincos(pos, a.freqs.w[k0 + 1], &s1, &c1);
+#pragma unroll
+      for (int u = 0; u < kMaxHeads; ++u) {
+        if (u >= nh) break;
+        uint16_t *kout = a.k_cache + (slot * a.Hkv + h0 + u) * D;
+        uint16_t *vout = a.v_cache + (slot * a.Hkv + h0 + u) * D;
+        const float a0 = dts::bf16_lo(k1[u]), a1 = dts::bf16_hi(k1[u]);
+        const float b0 = dts::bf16_lo(k2[u]), b1 = dts::bf16_hi(k2[u]);
+        reinterpret_cast<uint32_t *>(kout)[lane] = dts::pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
+        reinterpret_cast<uint32_t *>(kout + 64)[lane] = dts::pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+        reinterpret_cast<uint2 *>(vout)[lane] = v[u];
+      }
+    } else {
+      float s0, c0;
+      dts::rope_sincos(pos, a.freqs.w[lane], &s0, &c0);
+#pragma unroll
+      for (int u = 0; u < kMaxHeads; ++u) {
+        if (u >= nh) break;
+        uint16_t *kout = a.k_cache + (slot * a.Hkv + h0 + u) * D;
+        uint16_t *vout = a.v_cache + (slot * a.Hkv + h0 + u) * D;
+        const float a0 = __uint_as_float(k1[u] << 16);
+        const float b0 = __uint_as_float(k2[u] << 16);
+        const uint32_t r = dts::pack_bf16x2(a0 * c0 - b0 * s0, b0 * c0 + a0 * s0);
+        kout[lane] = static_cast<uint16_t>(r & 0xFFFFu);
+        kout[32 + lane] = static_cast<uint16_t>(r >> 16);
+        reinterpret_cast<uint32_t *>(vout)[lane] = v[u].x;
+      }
+    }
   }
 }
 
@@ -113,7 +140,7 @@ extern "C" int dts_write_window_kv(const uint16_t *k_new, const uint16_t *v_new,
   a.N = N;
   a.Hkv = Hkv;
   dts_host::make_rope_freqs(rope_theta, d, &a.freqs);
-  const int64_t warps = static_cast<int64_t>(B) * N * Hkv;
+  const int64_t warps = static_cast<int64_t>(B) * N;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (d == 128) write_window_kv_kernel<128><<<blocks, 256, 0, s>>>(a);
