@@ -92,77 +92,145 @@ __device__ void move_rows_any(char *base, int64_t stride, int row_bytes, const i
   else move_rows<uint32_t>(base, stride, row_bytes / 4, dst_slot, src_slot, n_moved);
 }
 
-// grid (n_buffers, B)
+constexpr int kBufPerBlock = 8;  // buffers of the table one block moves
+
+// grid (ceil(n_buffers / kBufPerBlock), B): the request's moves are collected
+// once and applied to kBufPerBlock buffers; when every one of them is 16-byte
+// aligned, all their moved rows go in one load-then-store round.
 __global__ void __launch_bounds__(kThreads) compact_window_rows_kernel(
     const dts_kv_buffer *__restrict__ table, int n_buffers, const int64_t *__restrict__ wl,
     const int32_t *__restrict__ accepted_path, const int32_t *__restrict__ accept_len, int N,
     int32_t *err) {
   __shared__ int s_dst[dts::kMaxNodes], s_src[dts::kMaxNodes];
   __shared__ int64_t s_dslot[dts::kMaxNodes], s_sslot[dts::kMaxNodes];
-  __shared__ int s_n, s_skip;
-  const int l = blockIdx.x;
+  __shared__ dts_kv_buffer s_e[kBufPerBlock];
+  __shared__ int s_skip[kBufPerBlock];
+  __shared__ int64_t s_pref[kBufPerBlock + 1];  // words (16-byte) before buffer k's rows
+  __shared__ int s_n, s_all16;
+  const int l0 = blockIdx.x * kBufPerBlock;
+  const int nb = min(kBufPerBlock, n_buffers - l0);
   const int b = blockIdx.y;
-  const dts_kv_buffer e = table[l];
-  if (threadIdx.x == 0) {
-    s_skip = 0;
-    const uint64_t a = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
-                       static_cast<uint64_t>(e.row_bytes);
-    if (e.base == nullptr || (a & 3) != 0 || e.row_bytes <= 0 || e.slot_stride_bytes < e.row_bytes ||
+  if (threadIdx.x < nb) {
+    const dts_kv_buffer e = table[l0 + threadIdx.x];
+    s_e[threadIdx.x] = e;
+    const uint64_t al = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
+                        static_cast<uint64_t>(e.row_bytes);
+    int skip = 0;
+    if (e.base == nullptr || (al & 3) != 0 || e.row_bytes <= 0 || e.slot_stride_bytes < e.row_bytes ||
         e.num_slots <= 0 || e.reserved != 0) {
       dts::report(err, DTS_DEV_BAD_BUFFER);
-      s_skip = 1;
+      skip = 1;
     }
+    s_skip[threadIdx.x] = skip;
   }
   __syncthreads();
-  if (s_skip) return;
-  // Each physical region moves once: skip this entry if another entry with the
+  // Each physical region moves once: skip an entry if another entry with the
   // same stride covers its rows (equal ranges: the lower index moves).
-  const uint64_t lo = reinterpret_cast<uint64_t>(e.base);
-  const uint64_t hi = lo + static_cast<uint64_t>(e.row_bytes);
-  for (int o = threadIdx.x; o < n_buffers; o += kThreads) {
-    if (o == l) continue;
+  for (int q = threadIdx.x; q < nb * n_buffers; q += kThreads) {
+    const int k = q / n_buffers, o = q - k * n_buffers;
+    const int l = l0 + k;
+    if (o == l || s_skip[k] == 1) continue;
+    const dts_kv_buffer e = s_e[k];
     const dts_kv_buffer f = table[o];
     if (f.slot_stride_bytes != e.slot_stride_bytes || f.base == nullptr) continue;
+    const uint64_t lo = reinterpret_cast<uint64_t>(e.base);
+    const uint64_t hi = lo + static_cast<uint64_t>(e.row_bytes);
     const uint64_t flo = reinterpret_cast<uint64_t>(f.base);
     const uint64_t fhi = flo + static_cast<uint64_t>(f.row_bytes);
-    if (fhi <= lo || hi <= flo) continue;                  // disjoint
+    if (fhi <= lo || hi <= flo) continue;                       // disjoint
     const bool inside = flo <= lo && hi <= fhi;
     const bool outside = lo <= flo && fhi <= hi;
-    if (inside && !(outside && o > l)) atomicOr(&s_skip, 1);  // covered by o
-    else if (!inside && !outside) atomicOr(&s_skip, 2);        // partial overlap
-  }
-  __syncthreads();
-  if (s_skip) {
-    if (threadIdx.x == 0 && (s_skip & 2) && b == 0) dts::report(err, DTS_DEV_BAD_BUFFER);
-    return;
+    if (inside && !(outside && o > l)) atomicOr(&s_skip[k], 2);  // covered by o
+    else if (!inside && !outside) atomicOr(&s_skip[k], 4);       // partial overlap
   }
   if (threadIdx.x < 32) {
     const int n = collect_moves_warp(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
     __syncwarp();
     if (n < 0) {
       if (threadIdx.x == 0) {
-        if (l == 0) dts::report(err, DTS_DEV_BAD_PATH);
+        if (blockIdx.x == 0) dts::report(err, DTS_DEV_BAD_PATH);
         s_n = 0;
       }
     } else {
-      bool bad = false;
       for (int m = threadIdx.x; m < n; m += 32) {
-        const int64_t d = wl[static_cast<int64_t>(b) * N + s_dst[m]];
-        const int64_t s = wl[static_cast<int64_t>(b) * N + s_src[m]];
-        bad |= d < 0 || d >= e.num_slots || s < 0 || s >= e.num_slots;
-        s_dslot[m] = d;
-        s_sslot[m] = s;
+        s_dslot[m] = wl[static_cast<int64_t>(b) * N + s_dst[m]];
+        s_sslot[m] = wl[static_cast<int64_t>(b) * N + s_src[m]];
       }
-      bad = __any_sync(0xffffffffu, bad);
-      if (threadIdx.x == 0) {
-        if (bad) dts::report(err, DTS_DEV_BAD_SLOT);
-        s_n = bad ? 0 : n;
-      }
+      if (threadIdx.x == 0) s_n = n;
     }
   }
   __syncthreads();
-  if (s_n == 0) return;
-  move_rows_any(static_cast<char *>(e.base), e.slot_stride_bytes, e.row_bytes, s_dslot, s_sslot, s_n);
+  const int n_moved = s_n;
+  if (n_moved == 0) return;
+  if (threadIdx.x < nb) {
+    // slots in range for this buffer, the overlap verdicts, 16-byte words
+    const dts_kv_buffer e = s_e[threadIdx.x];
+    int skip = s_skip[threadIdx.x];
+    if (skip & 4) {
+      if (b == 0) dts::report(err, DTS_DEV_BAD_BUFFER);
+    }
+    if (skip == 0) {
+      bool bad = false;
+      for (int m = 0; m < n_moved; ++m)
+        bad |= s_dslot[m] < 0 || s_dslot[m] >= e.num_slots || s_sslot[m] < 0 || s_sslot[m] >= e.num_slots;
+      if (bad) {
+        dts::report(err, DTS_DEV_BAD_SLOT);
+        skip = 8;
+      }
+    }
+    s_skip[threadIdx.x] = skip;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t acc = 0;
+    int all16 = 1;
+    for (int k = 0; k < nb; ++k) {
+      s_pref[k] = acc;
+      if (s_skip[k] != 0) continue;
+      const dts_kv_buffer e = s_e[k];
+      const uint64_t al = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
+                          static_cast<uint64_t>(e.row_bytes);
+      all16 &= (al & 15) == 0 ? 1 : 0;
+      acc += static_cast<int64_t>(n_moved) * (e.row_bytes / 16);
+    }
+    s_pref[nb] = acc;
+    s_all16 = all16;
+  }
+  __syncthreads();
+  if (!s_all16) {
+    for (int k = 0; k < nb; ++k)
+      if (s_skip[k] == 0)
+        move_rows_any(static_cast<char *>(s_e[k].base), s_e[k].slot_stride_bytes, s_e[k].row_bytes, s_dslot,
+                      s_sslot, n_moved);
+    return;
+  }
+  // every moved row of every buffer, as 16-byte words, in rounds
+  const int64_t total = s_pref[nb];
+  for (int64_t r0 = 0; r0 < total; r0 += static_cast<int64_t>(kThreads) * kPerThread) {
+    uint4 v[kPerThread];
+    char *dst_addr[kPerThread];
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q) {
+      const int64_t e = r0 + static_cast<int64_t>(q) * kThreads + threadIdx.x;
+      dst_addr[q] = nullptr;
+      if (e < total) {
+        int k = 0;
+        while (k + 1 < nb && s_pref[k + 1] <= e) ++k;
+        const int64_t row_words = s_e[k].row_bytes / 16;
+        const int64_t local = e - s_pref[k];
+        const int m = static_cast<int>(local / row_words);
+        const int64_t c = local - m * row_words;
+        char *base = static_cast<char *>(s_e[k].base);
+        v[q] = reinterpret_cast<const uint4 *>(base + s_sslot[m] * s_e[k].slot_stride_bytes)[c];
+        dst_addr[q] = base + s_dslot[m] * s_e[k].slot_stride_bytes + c * 16;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q)
+      if (dst_addr[q] != nullptr) *reinterpret_cast<uint4 *>(dst_addr[q]) = v[q];
+    __syncthreads();
+  }
 }
 
 // grid (B)
@@ -203,7 +271,8 @@ extern "C" int dts_compact_window_rows(const dts_kv_buffer *table, int n_buffers
   if (B == 0 || n_buffers == 0) return DTS_OK;
   if (n_buffers > 65535 || B > 65535) return DTS_ERR_UNSUPPORTED;
   if (!table || !write_locations || !accepted_path || !accept_len) return DTS_ERR_INVALID;
-  compact_window_rows_kernel<<<dim3(n_buffers, B), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  const int groups = (n_buffers + kBufPerBlock - 1) / kBufPerBlock;
+  compact_window_rows_kernel<<<dim3(groups, B), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       table, n_buffers, write_locations, accepted_path, accept_len, N, err_dev);
   return dts_host::launch_status();
 }
