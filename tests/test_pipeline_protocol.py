@@ -1,159 +1,198 @@
 """A CPU model of the tree-attention kernel's mbarrier pipeline, run over
-random schedules: it must never deadlock.
+random schedules: it must never deadlock, every parity wait must be sound, and
+no load may land in a buffer that a queued MMA has still to read.
 
 The model mirrors the roles of one CTA of the tensor-core tree pass: the TMA
-producer (Q tile, then K and V tiles of a ring of slots), the MMA issuer, the
-V-tile warp (hands each V tile to the MMA issuer) and the two softmax groups,
-plus the asynchronous engines (TMA copies complete after random delays, the
-tensor core runs its queue in order). A barrier counts completed phases; a
-parity wait passes when the current phase's parity differs from the one
-named, which is only sound while the waiter is at most one phase behind.
+producer (Q tiles, then K and V tiles of a ring of slots), the MMA issuer (per
+key tile j and row tile t: PV_t(j), then S_t(j+1), which overwrites P_t(j)
+only after PV_t(j) read it), the V-tile warp (hands each V tile to the MMA
+issuer, publishes the segment's poison mask) and the two softmax groups, plus
+the asynchronous engines: TMA copies land after random delays and the tensor
+core runs the issuer's MMAs and commits in order.
 
-Two variants of the V-tile warp that an earlier form of the kernel used are
-kept as mutants: waiting on a barrier shared by K and V loads (both only for
-the V phases, and for every phase in order) deadlocks on some schedules, and
-the model has to catch both.
+A barrier counts completed phases. Every arrival names the phase it belongs
+to, and the model checks it against the barrier's current phase. A parity
+wait passes when the current phase's parity differs from the one named; the
+model checks at every evaluation that the waiter is at most one phase behind,
+the condition under which the hardware's answer is the intended one. The
+model also tracks which buffers (Q tiles, ring slots) queued MMAs have still
+to read, and fails if a load lands in one of them first.
+
+Mutants the model has to catch: V-tile warps that wait on a barrier shared by
+K and V loads (only for the V phases, or for every phase in order), a V slot
+released after the first row tile's PV instead of the last, and the Q tiles
+released after a segment's second S instead of its last.
 """
+import collections
 import random
 
 import pytest
 
 
-class _Bar:
-    def __init__(self, count):
-        self.count, self.pend, self.done = count, 0, 0
+class ProtocolError(AssertionError):
+    pass
 
-    def arrive(self, k=1):
+
+class _Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pend, self.done = name, count, 0, 0
+
+    def arrive(self, phase, k=1):
+        if phase != self.done:
+            raise ProtocolError(f"{self.name}: arrival for phase {phase} while in phase {self.done}")
         self.pend += k
-        assert self.pend <= self.count
+        if self.pend > self.count:
+            raise ProtocolError(f"{self.name}: too many arrivals")
         if self.pend == self.count:
             self.pend = 0
             self.done += 1
 
-    def passes(self, parity):
-        return (self.done & 1) != parity
+    def passes(self, phase):
+        if self.done > phase + 1:
+            raise ProtocolError(f"{self.name}: waiter of phase {phase} two phases behind ({self.done} done)")
+        return (self.done & 1) != (phase & 1)
 
 
-def _kind_phase(use, slots):
+def _kind_index(use, slots):
+    """Phase index of `use` on its slot's K (even uses) or V (odd uses)
+    barrier: with an even ring a slot holds one kind, with an odd ring the
+    kinds alternate by round."""
     rnd = use // slots
-    return (rnd if slots % 2 == 0 else rnd >> 1) & 1
+    return rnd if slots % 2 == 0 else rnd >> 1
 
 
-def _simulate(segs, slots, seed, v_warp="split", slow_v_warp=False, max_steps=400000):
-    """segs: (key tiles, row tiles) per segment. Returns None when every role
-    finishes, else the blocked waits."""
+def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=600000):
+    """segs: (key tiles, row tiles present) per segment. Returns None when
+    every role finishes, else the blocked waits; raises ProtocolError on an
+    unsound step."""
     rng = random.Random(seed)
     bars = {}
+    shared = mutant in ("shared_v_only", "shared_all")
 
     def bar(name, count=1):
-        bars.setdefault(name, _Bar(count))
-        return bars[name]
+        bars[name] = _Bar(name, count)
 
     for s in range(slots):
-        for n in ("full", "kfull", "vfull", "empty", "vready"):
+        for n in ("full", "kfull", "vfull", "vready", "empty"):
             bar(f"{n}{s}")
     for t in range(2):
         bar(f"s_full{t}"), bar(f"p_full{t}", 128), bar(f"o_fin{t}"), bar(f"o_free{t}", 128)
     bar("q_full"), bar("q_empty"), bar("win_bar")
-    tma, tensor_q = [], []
-    split = v_warp == "split"
+    tma = []                       # [delay, barrier, phase]
+    tensor_q = []                  # the issuer's MMAs and commits, run in order
+    reads = collections.Counter()  # buffers that queued MMAs have still to read
+
+    def mma_op(*bufs):
+        for b in bufs:
+            reads[b] += 1
+        tensor_q.append(("op", bufs))
+
+    def commit(name, phase):
+        tensor_q.append(("commit", name, phase))
+
+    def overwrite(buf):
+        # a load may land in a buffer only once every MMA that reads its old contents has run
+        if reads[buf]:
+            raise ProtocolError(f"{buf} overwritten while an MMA still has to read it")
 
     def load_done(use):
-        if not split:
-            return f"full{use % slots}"
-        return f"{'v' if use & 1 else 'k'}full{use % slots}"
+        if shared:
+            return f"full{use % slots}", use // slots
+        return f"{'v' if use & 1 else 'k'}full{use % slots}", _kind_index(use, slots)
 
     def k_wait(use):
-        if split:
-            return ("wait", f"kfull{use % slots}", _kind_phase(use, slots))
-        return ("wait", f"full{use % slots}", (use // slots) & 1)
+        name, ph = load_done(use)
+        return ("wait", name, ph)
 
     def producer():
-        use = segc = 0
-        for nkt, _ in segs:
-            yield ("wait", "q_empty", (segc & 1) ^ 1)
-            tma.append([rng.randint(1, 30), "q_full"])
-            segc += 1
+        use = 0
+        for segc, (nkt, _) in enumerate(segs):
+            yield ("wait", "q_empty", segc - 1)
+            overwrite(("q", segc - 1))
+            tma.append([rng.randint(1, 30), "q_full", segc])
             for _ in range(2 * nkt):
-                yield ("wait", f"empty{use % slots}", ((use // slots) & 1) ^ 1)
-                tma.append([rng.randint(1, 30), load_done(use)])
+                yield ("wait", f"empty{use % slots}", use // slots - 1)
+                overwrite(("kv", use - slots))
+                tma.append([rng.randint(1, 30), *load_done(use)])
                 use += 1
 
     def mma():
-        use = segc = 0
+        use = 0
         tcnt, scnt = [0, 0], [0, 0]
-        for nkt, nt in segs:
-            yield ("wait", "q_full", segc & 1)
+        for segc, (nkt, nt) in enumerate(segs):
+            yield ("wait", "q_full", segc)
             yield k_wait(use)
             for t in range(nt):
-                tensor_q.append(("commit", f"s_full{t}"))
+                mma_op(("q", segc), ("kv", use))
+                commit(f"s_full{t}", tcnt[t])
             if nkt == 1:
-                tensor_q.append(("commit", "q_empty"))
-            tensor_q.append(("commit", f"empty{use % slots}"))
+                commit("q_empty", segc)
+            commit(f"empty{use % slots}", use // slots)
             for j in range(nkt):
                 vuse, kuse, more = use + 2 * j + 1, use + 2 * j + 2, j + 1 < nkt
-                yield ("wait", f"vready{vuse % slots}", _kind_phase(vuse, slots))
+                yield ("wait", f"vready{vuse % slots}", _kind_index(vuse, slots))
                 if more:
                     yield k_wait(kuse)
                 for t in range(nt):
-                    yield ("wait", f"p_full{t}", (tcnt[t] + j) & 1)
+                    yield ("wait", f"p_full{t}", tcnt[t] + j)
                     if j == 0 and scnt[t] > 0:
-                        yield ("wait", f"o_free{t}", (scnt[t] - 1) & 1)
-                    tensor_q.append(("op",))
-                    if t == nt - 1:
-                        tensor_q.append(("commit", f"empty{vuse % slots}"))
+                        yield ("wait", f"o_free{t}", scnt[t] - 1)
+                    mma_op(("kv", vuse))
                     if more:
-                        tensor_q.append(("commit", f"s_full{t}"))
+                        mma_op(("q", segc), ("kv", kuse))
+                    v_release_at = 0 if mutant == "early_v_release" else nt - 1
+                    if t == v_release_at:
+                        commit(f"empty{vuse % slots}", vuse // slots)
+                    if more:
+                        commit(f"s_full{t}", tcnt[t] + j + 1)
                         if t == nt - 1:
-                            if j + 2 == nkt:
-                                tensor_q.append(("commit", "q_empty"))
-                            tensor_q.append(("commit", f"empty{kuse % slots}"))
+                            q_release_at = 0 if mutant == "early_q_release" else nkt - 2
+                            if j == q_release_at:
+                                commit("q_empty", segc)
+                            commit(f"empty{kuse % slots}", kuse // slots)
                     else:
-                        tensor_q.append(("commit", f"o_fin{t}"))
+                        commit(f"o_fin{t}", scnt[t])
             use += 2 * nkt
             for t in range(nt):
                 tcnt[t] += nkt
                 scnt[t] += 1
-            segc += 1
 
     def v_tile_warp():
         use, prev_nt, scnt = 0, 0, [0, 0]
-        for nkt, nt in segs:
+        for segc, (nkt, nt) in enumerate(segs):
             for j in range(nkt):
                 kuse, vuse = use + 2 * j, use + 2 * j + 1
-                if v_warp == "split":
-                    yield ("wait", f"vfull{vuse % slots}", _kind_phase(vuse, slots))
-                elif v_warp == "shared_v_only":
-                    yield ("wait", f"full{vuse % slots}", (vuse // slots) & 1)
-                else:  # shared, every phase in order
-                    yield ("wait", f"full{kuse % slots}", (kuse // slots) & 1)
-                    yield ("wait", f"full{vuse % slots}", (vuse // slots) & 1)
-                bars[f"vready{vuse % slots}"].arrive()
+                if mutant == "shared_v_only":
+                    yield ("wait", f"full{vuse % slots}", vuse // slots)
+                elif mutant == "shared_all":
+                    yield ("wait", f"full{kuse % slots}", kuse // slots)
+                    yield ("wait", f"full{vuse % slots}", vuse // slots)
+                else:
+                    yield ("wait", f"vfull{vuse % slots}", _kind_index(vuse, slots))
+                bars[f"vready{vuse % slots}"].arrive(_kind_index(vuse, slots))
                 yield ("step",)
             for t in range(2):
                 if t < prev_nt and scnt[t] > 0:
-                    yield ("wait", f"o_free{t}", (scnt[t] - 1) & 1)
+                    yield ("wait", f"o_free{t}", scnt[t] - 1)
             prev_nt = nt
             for t in range(nt):
                 scnt[t] += 1
-            bars["win_bar"].arrive()
+            bars["win_bar"].arrive(segc)
             use += 2 * nkt
 
     def softmax(t):
-        tcnt = scnt = wcnt = 0
-        for nkt, nt in segs:
-            wpar = wcnt & 1
-            wcnt += 1
+        tcnt = scnt = 0
+        for segc, (nkt, nt) in enumerate(segs):
             if t >= nt:
                 continue
             for j in range(nkt):
-                yield ("wait", f"s_full{t}", (tcnt + j) & 1)
+                yield ("wait", f"s_full{t}", tcnt + j)
                 yield ("step",)
-                bars[f"p_full{t}"].arrive(128)
-            yield ("wait", f"o_fin{t}", scnt & 1)
-            yield ("wait", "win_bar", wpar)
+                bars[f"p_full{t}"].arrive(tcnt + j, 128)
+            yield ("wait", f"o_fin{t}", scnt)
+            yield ("wait", "win_bar", segc)
             yield ("step",)
-            bars[f"o_free{t}"].arrive(128)
+            bars[f"o_free{t}"].arrive(scnt, 128)
             tcnt += nkt
             scnt += 1
 
@@ -165,11 +204,14 @@ def _simulate(segs, slots, seed, v_warp="split", slow_v_warp=False, max_steps=40
             e[0] -= 1
         for e in [e for e in tma if e[0] <= 0]:
             tma.remove(e)
-            bars[e[1]].arrive()
+            bars[e[1]].arrive(e[2])
         if tensor_q and rng.random() < 0.5:
             op = tensor_q.pop(0)
             if op[0] == "commit":
-                bars[op[1]].arrive()
+                bars[op[1]].arrive(op[2])
+            else:
+                for b in op[1]:
+                    reads[b] -= 1
         ready = [k for k in roles if k not in done and (pending[k] is None or bars[pending[k][1]].passes(pending[k][2]))]
         if not ready:
             if not tma and not tensor_q:
@@ -194,15 +236,23 @@ def _cases(n, seed0):
         yield segs, rng.choice([5, 8]), seed0 + i, i % 2 == 0
 
 
-def test_pipeline_never_deadlocks():
+def test_pipeline_never_deadlocks_and_waits_are_sound():
     stuck = [(segs, slots, seed) for segs, slots, seed, slow in _cases(120, 7000)
-             if _simulate(segs, slots, seed, "split", slow) is not None]
+             if _simulate(segs, slots, seed, None, slow) is not None]
     assert not stuck, stuck[:3]
 
 
-@pytest.mark.parametrize("variant", ["shared_v_only", "shared_all"])
-def test_model_catches_shared_barrier_variants(variant):
-    """Each flawed V-tile warp deadlocks on some schedule: the model can see
-    the failure the split barriers remove."""
-    found = any(_simulate(segs, slots, seed, variant, slow) is not None for segs, slots, seed, slow in _cases(160, 9100))
-    assert found
+@pytest.mark.parametrize("mutant", ["shared_v_only", "shared_all", "early_v_release", "early_q_release"])
+def test_model_catches_protocol_mutants(mutant):
+    """Each flawed protocol breaks on some schedule: an arrival for a phase
+    the barrier is not in, a waiter two phases behind, a load over a buffer
+    still to be read, or a deadlock."""
+    caught = False
+    for segs, slots, seed, slow in _cases(200, 9100):
+        try:
+            caught = _simulate(segs, slots, seed, mutant, slow) is not None
+        except ProtocolError:
+            caught = True
+        if caught:
+            break
+    assert caught
