@@ -23,6 +23,7 @@ pages print, closed forms, invariants or brute force (tests/test_oracle_*.py).
 Modules: ``tree`` (validation, ancestor mask, positions, links), ``rope``,
 ``attention`` (per-path literal attention), ``walk`` (greedy verification),
 ``compact`` (KV-row / hidden-row / position compaction), ``merge`` (the
-log-sum-exp combine rule).
+log-sum-exp combine rule), ``argmax`` (the target's argmax per verify row and
+the walk fed by it).
 """
-from . import tree, rope, attention, walk, compact, merge  # noqa: F401
+from . import tree, rope, attention, walk, compact, merge, argmax  # noqa: F401

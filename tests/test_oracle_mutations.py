@@ -171,3 +171,30 @@ def test_compact_and_merge_mutations_caught(monkeypatch):
                         lambda outs, ls: (np.mean(np.asarray(outs, float), axis=0), np.max(ls, axis=0)))
     assert _fails(PA.test_merge_scalar_example, load_golden)
     assert math.isfinite(1.0)
+
+
+def _argmax_last_of_ties(logits):
+    x = np.asarray(logits)
+    return (x.shape[1] - 1 - np.argmax(x[:, ::-1], axis=1)).astype(np.int32)
+
+
+def _argmax_ignoring_nan(logits):
+    x = np.asarray(logits, dtype=np.float64)
+    x = np.where(np.isnan(x), -np.inf, x)
+    return np.argmax(x, axis=1).astype(np.int32)
+
+
+def _argmax_of_column(logits):  # a transposed operand: argmax down the columns
+    x = np.asarray(logits)
+    return np.resize(np.argmax(x, axis=0), x.shape[0]).astype(np.int32)
+
+
+def test_argmax_mutations_caught(monkeypatch):
+    import oracle.argmax as AM
+    from tests import test_oracle_argmax as PM
+    for bad in (_argmax_last_of_ties, _argmax_ignoring_nan, _argmax_of_column):
+        monkeypatch.setattr(AM, "row_argmax", bad)
+        caught = _fails(PM.test_matches_plain_scan_with_many_ties)
+        for row, expect in ([[2.0, math.nan, 9.0, math.nan], 1], [[1.0, 7.0, 3.0, 7.0], 1]):
+            caught = caught or _fails(PM.test_special_cases, row, expect)
+        assert caught, bad.__name__
