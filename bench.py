@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--workload", default="eagle2_p8192_n64", choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-argmax", action="store_true", help="skip the target-argmax measurement")
     return ap.parse_args()
 
 
@@ -372,6 +373,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if not args.no_argmax:
+        line["target_argmax"] = time_target_argmax(inp, db, stream, flush, args, hbm)
     clocks = clk.summary()
     if clocks is not None:
         line["clocks"] = clocks
@@ -381,6 +384,46 @@ def run_ours(args, rank, world, local_rank):
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle",
                                 "sample": sample, "seconds": dt}
     return line
+
+
+def time_target_argmax(inp, db, stream, flush, args, hbm):
+    """The target's argmax over the workload's fp32 logits [B*N][vocab] and the
+    walk fed by it (dts_verify_tree_greedy_logits), outside the headline step:
+    CUDA-event time of the argmax call alone and of the fused call, L2 flushed
+    before each; the argmax streams the logits once, so its roofline is HBM."""
+    import torch
+    from draft_tree_speculative_gb300 import target_argmax, target_argmax_workspace, verify_tree_greedy_logits
+    w = inp.w
+    rows = w.B * w.N
+    logits = torch.from_numpy(synth.target_logits(w, inp.target_argmax)).to(db.device)
+    arg = torch.empty((w.B, w.N), dtype=torch.int32, device=db.device)
+    ws = torch.empty(max(8, target_argmax_workspace(rows, w.vocab)), dtype=torch.uint8, device=db.device)
+    reps = max(5, min(args.steps, 50))
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            for a, b in ev:
+                flush.fill_(1)
+                a.record(stream)
+                fn()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
+
+    us = timed(lambda: target_argmax(logits, arg.view(-1), ws, stream=stream))
+    fused_us = timed(lambda: verify_tree_greedy_logits(db.draft, logits, arg, db.accept_len, db.accepted_path,
+                                                       db.accepted_tokens, ws, parents=db.parents, err=db.err,
+                                                       stream=stream))
+    check_device_error(db, "the argmax and walk")
+    ok = bool((arg.cpu().numpy() == inp.target_argmax).all())
+    nbytes = rows * w.vocab * 4
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"us": us, "fused_walk_us": fused_us, "rows": rows, "vocab": w.vocab, "bytes": nbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm},
+            "argmax_matches_planted_target": ok, "reps": reps}
 
 
 def run_reference(args):

@@ -25,7 +25,8 @@ EXPORTED = (
     "dts_version", "dts_status_string", "dts_device_error_string", "dts_build_tree_mask",
     "dts_write_window_kv", "dts_tree_verify_attention_workspace", "dts_tree_verify_attention",
     "dts_verify_tree_greedy", "dts_compact_window_rows", "dts_compact_rows",
-    "dts_tree_verify_attention_static_ws",
+    "dts_tree_verify_attention_static_ws", "dts_target_argmax_workspace", "dts_target_argmax",
+    "dts_verify_tree_greedy_logits",
 )
 
 
@@ -55,6 +56,9 @@ _SIGS = {
     "dts_tree_verify_attention_static_ws": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I,
                                                  _F, _P, _P, _P, _P]),
     "dts_verify_tree_greedy": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
+    "dts_target_argmax_workspace": (_SZ, [_L, _I]),
+    "dts_target_argmax": (_I, [_P, _L, _I, _L, _P, _P, _SZ, _P]),
+    "dts_verify_tree_greedy_logits": (_I, [_P, _P, _I, _L, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "dts_compact_window_rows": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P]),
     "dts_compact_rows": (_I, [_P, _L, _P, _P, _P, _P, _I, _I, _P, _P]),
 }
@@ -244,6 +248,53 @@ def verify_tree_greedy(draft_tokens, target_argmax, accept_len, accepted_path, a
                                       _ptr(next_sibling), B, N, _ptr(accept_len), _ptr(accepted_path),
                                       _ptr(accepted_tokens), _ptr(err), _stream(stream))
     _raise(st, "verify_tree_greedy")
+
+
+def _logits(logits):
+    """(pointer, rows, vocab, row stride) of fp32 logits [rows][vocab] whose
+    rows may be strided (each row's vocab entries contiguous)."""
+    torch = _torch()
+    if logits.dtype != torch.float32 or logits.dim() != 2:
+        raise TypeError("logits: expected a 2-D float32 tensor")
+    if not logits.is_cuda:
+        raise ValueError("logits: expected a CUDA tensor")
+    if logits.shape[1] > 1 and logits.stride(1) != 1:
+        raise ValueError("logits: each row must be contiguous")
+    return logits.data_ptr(), logits.shape[0], logits.shape[1], logits.stride(0)
+
+
+def target_argmax_workspace(rows, vocab) -> int:
+    return int(lib().dts_target_argmax_workspace(int(rows), int(vocab)))
+
+
+def target_argmax(logits, argmax, workspace, stream=None):
+    """argmax [rows] int32 <- the index of each row's largest logit."""
+    p, rows, vocab, stride = _logits(logits)
+    _check(argmax, _i32(), (rows,), "argmax")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().dts_target_argmax(p, rows, vocab, stride, _ptr(argmax), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise(st, "target_argmax")
+
+
+def verify_tree_greedy_logits(draft_tokens, logits, target_argmax, accept_len, accepted_path, accepted_tokens,
+                              workspace, parents=None, next_token=None, next_sibling=None, err=None, stream=None):
+    """The argmax of logits [B*N][vocab] into target_argmax [B][N], then the greedy walk."""
+    B, N = draft_tokens.shape
+    p, rows, vocab, stride = _logits(logits)
+    if rows != B * N:
+        raise ValueError("logits must have B*N rows")
+    i32 = _i32()
+    for name, t in (("draft_tokens", draft_tokens), ("target_argmax", target_argmax), ("parents", parents),
+                    ("next_token", next_token), ("next_sibling", next_sibling),
+                    ("accepted_path", accepted_path), ("accepted_tokens", accepted_tokens)):
+        _check(t, i32, (B, N), name)
+    _check(accept_len, i32, (B,), "accept_len")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().dts_verify_tree_greedy_logits(_ptr(draft_tokens), p, vocab, stride, _ptr(parents), _ptr(next_token),
+                                             _ptr(next_sibling), B, N, _ptr(target_argmax), _ptr(accept_len),
+                                             _ptr(accepted_path), _ptr(accepted_tokens), _ptr(workspace), ws_bytes,
+                                             _ptr(err), _stream(stream))
+    _raise(st, "verify_tree_greedy_logits")
 
 
 def make_kv_table(entries: Sequence, device="cuda"):

@@ -36,7 +36,7 @@ ROPE_THETA = 5.0e5
 
 # Child-stream order; never reorder (it would change every stored value).
 _STREAMS = ("tree", "tokens", "q", "k_cache", "v_cache", "k_new", "v_new",
-            "pages", "hidden", "fp8", "prefix")
+            "pages", "hidden", "fp8", "prefix", "logits")
 
 
 @dataclasses.dataclass(frozen=True)
@@ -375,6 +375,22 @@ def make_inputs(w: Workload, with_cache: bool = True, with_hidden: bool = True,
         k_cache = v_cache = None
     hidden = normal_bf16(s["hidden"], (BN, w.hidden_dim)) if with_hidden else None
     return VerifyInputs(w, parents, depth, draft, argmax, lay, q, k_new, v_new, k_cache, v_cache, hidden)
+
+
+# A logit no N(0,1) draw comes near (P(N(0,1) > 20) is about 3e-89).
+PLANTED_LOGIT = 20.0
+
+
+def target_logits(w: Workload, target_argmax: np.ndarray) -> np.ndarray:
+    """fp32 target logits [B*N][vocab] for the verify rows: iid N(0,1) draws,
+    with each row's entry at that row's drawn target token set to
+    PLANTED_LOGIT, so the target tokens drawn by make_tokens (and the drafts
+    made from them) are the rows' argmax by construction."""
+    rng = streams(w.index)["logits"]
+    rows = w.B * w.N
+    x = rng.standard_normal((rows, w.vocab), dtype=np.float32)
+    x[np.arange(rows), np.asarray(target_argmax).reshape(-1)] = PLANTED_LOGIT
+    return x
 
 
 def fp8_window_rows(w: Workload, n_buffers: int, row_bytes: int) -> np.ndarray:

@@ -11,6 +11,8 @@
  *   dts_tree_verify_attention   every row attends the committed prefix plus
  *                               its own ancestors; out + base-2 LSE
  *   dts_verify_tree_greedy      greedy walk -> accept_len, packed path, tokens
+ *   dts_target_argmax           the target's argmax per verify row (and
+ *   dts_verify_tree_greedy_logits  that argmax fed straight into the walk)
  *   dts_compact_window_rows     the path's KV rows -> the window's front slots
  *   dts_compact_rows            the path's hidden rows -> the front; positions
  *                               back to vc + i
@@ -240,6 +242,56 @@ int dts_verify_tree_greedy(const int32_t *draft_tokens, const int32_t *target_ar
                            const int32_t *next_sibling, int B, int N, int32_t *accept_len,
                            int32_t *accepted_path, int32_t *accepted_tokens,
                            int32_t *err_dev, dts_stream_t stream);
+
+/*
+ * dts_target_argmax_workspace - bytes of scratch dts_target_argmax and
+ * dts_verify_tree_greedy_logits need for `rows` rows of `vocab` logits
+ * (8 bytes per row and 16384-logit chunk), or 0 for rows < 0 or vocab < 1.
+ */
+size_t dts_target_argmax_workspace(int64_t rows, int vocab);
+
+/*
+ * dts_target_argmax - the target's argmax at every verify row.
+ *
+ * Defined by [MI] "Walking the accepted path": the walk compares the draft
+ * tokens with the target's argmax at each node's position, computed for all
+ * nodes by the one verify forward; [MI], the worked (5, 4, 8) iteration, step
+ * 5: the argmax over all rows, then the walk.
+ *
+ *   logits     float [rows][row_stride]  row r's vocab logits at r * row_stride
+ *              (row_stride >= vocab, in elements; 4-byte aligned; rows that
+ *              start on 16-byte boundaries are read as float4 words)
+ *   argmax     int32 [rows]              out: index of the row's largest logit
+ *   workspace  device scratch of dts_target_argmax_workspace(rows, vocab)
+ *              bytes, 8-byte aligned, owned by the caller; nothing in it needs
+ *              to start at zero, and it is free again when the call's work on
+ *              `stream` has finished
+ *
+ * Ties go to the lowest index; a NaN counts as larger than any number (the
+ * first NaN of a row wins); -0.0 equals +0.0. Returns DTS_ERR_INVALID for a
+ * bad shape, pointer or alignment, DTS_ERR_WORKSPACE for a missing or small
+ * workspace, DTS_ERR_UNSUPPORTED when rows x chunks reaches 2^31.
+ */
+int dts_target_argmax(const float *logits, int64_t rows, int vocab, int64_t row_stride,
+                      int32_t *argmax, void *workspace, size_t ws_bytes, dts_stream_t stream);
+
+/*
+ * dts_verify_tree_greedy_logits - the target's argmax at every verify row
+ * (dts_target_argmax over logits [B*N][row_stride], row b*N+i for node i of
+ * request b) written to target_argmax [B][N], then dts_verify_tree_greedy
+ * over it, in one call on `stream` (sources as for those two calls).
+ *
+ * Every other argument, output and error is as for dts_target_argmax and
+ * dts_verify_tree_greedy; workspace is dts_target_argmax_workspace(B*N, vocab)
+ * bytes.
+ */
+int dts_verify_tree_greedy_logits(const int32_t *draft_tokens, const float *logits, int vocab,
+                                  int64_t row_stride, const int32_t *parents,
+                                  const int32_t *next_token, const int32_t *next_sibling, int B,
+                                  int N, int32_t *target_argmax, int32_t *accept_len,
+                                  int32_t *accepted_path, int32_t *accepted_tokens,
+                                  void *workspace, size_t ws_bytes, int32_t *err_dev,
+                                  dts_stream_t stream);
 
 /*
  * One K or V buffer of one layer (an entry of a cache group's address table).

@@ -66,3 +66,23 @@ def test_validation_before_launch(lib):
                                        128, 0.0, None, None, None, 0, None, None) == dts.ERR_UNSUPPORTED
     assert L.dts_tree_verify_attention(None, None, None, 100, None, 4, 64, None, 0, None, None, 5e5, 1, 8, 30, 8,
                                        128, 0.0, None, None, None, 0, None, None) == dts.ERR_INVALID
+
+
+def test_argmax_host_checks(lib):
+    L = dts.lib()
+    # 8 bytes per row and 16384-logit chunk
+    assert dts.target_argmax_workspace(2048, 128256) == 2048 * 8 * 8
+    assert dts.target_argmax_workspace(5, 1000) == 5 * 8
+    assert dts.target_argmax_workspace(3, 16385) == 3 * 2 * 8
+    assert dts.target_argmax_workspace(-1, 10) == 0 and dts.target_argmax_workspace(4, 0) == 0
+    # bad shapes and pointers fail before any launch; zero rows launch nothing
+    assert L.dts_target_argmax(None, 0, 10, 10, None, None, 0, None) == dts.OK
+    assert L.dts_target_argmax(None, 4, 10, 9, None, None, 0, None) == dts.ERR_INVALID      # row_stride < vocab
+    assert L.dts_target_argmax(None, 4, 10, 10, None, None, 0, None) == dts.ERR_INVALID     # null logits
+    assert L.dts_target_argmax(4096, 4, 10, 10, 8192, None, 0, None) == dts.ERR_WORKSPACE   # no workspace
+    assert L.dts_target_argmax(4098, 4, 10, 10, 8192, 65536, 4096, None) == dts.ERR_INVALID  # logits not 4-byte aligned
+    assert L.dts_target_argmax(4096, 4, 10, 10, 8192, 65537, 4096, None) == dts.ERR_INVALID  # workspace not 8-byte aligned
+    assert L.dts_verify_tree_greedy_logits(None, None, 10, 10, None, None, None, 2, 65, None, None, None, None, None,
+                                           0, None, None) == dts.ERR_UNSUPPORTED
+    assert L.dts_verify_tree_greedy_logits(None, None, 10, 10, None, None, None, 2, 8, None, None, None, None, None,
+                                           0, None, None) == dts.ERR_INVALID
