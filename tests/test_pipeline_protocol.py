@@ -248,7 +248,7 @@ def test_model_catches_protocol_mutants(mutant):
     the barrier is not in, a waiter two phases behind, a load over a buffer
     still to be read, or a deadlock."""
     caught = False
-    for segs, slots, seed, slow in _cases(200, 9100):
+    for segs, slots, seed, slow in _cases(800, 9100):
         try:
             caught = _simulate(segs, slots, seed, mutant, slow) is not None
         except ProtocolError:
