@@ -141,3 +141,72 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, page_table, prefix_len, 
                     out[b * N + v, hs] = o / Z[:, None]
                     lse2[b * N + v, hs] = (m[:, 0] + np.log(Z)) / LN2
     return out, lse2
+
+
+def window_attention(q, k_cache, v_cache, page_table, prefix_len, mask, positions, W: int, Hkv: int,
+                     theta: float, page_size: int = 64, scale: Optional[float] = None,
+                     q_rotated: bool = False, rope_out: Optional[str] = "bf16"):
+    """Attention of R query rows per request over the committed prefix plus
+    a masked window of W keys, all read from the paged cache.
+
+    Definition followed ([TS] "One tree attention": every row sees the
+    committed prefix, and the 64-bit ancestor mask applies only to the last
+    W keys; verify runs with R = W = N, draft lanes with R = K rows over the
+    (S - 1) * K-key lane window; [TS] "Draft lanes write the draft cache like
+    any draft step": every lane row sees the accepted frontier and, inside the
+    window, only its ancestors' slots, the lane mask):
+
+      keys(b, r) = [K_cache(b, p) for p < P]
+                   ++ [K_cache(b, P + j) for j < W with bit j of mask[b][r] set]
+      values     = the same positions of V_cache
+      q          = RoPE(q_raw[b*R + r, h], positions[b][r]), rounded as in
+                   verify_attention (``rope_out``)
+      out, lse2  = softmax over the keys (scale 1/sqrt(d)), base-2 LSE
+
+    The window keys are taken as the cache holds them (already rotated by the
+    step that wrote them); the oracle builds each row's key list itself and
+    never reads a path. Shapes: q [B*R][Hq][d]; k_cache, v_cache
+    [slots][Hkv][d]; page_table [B][max_pages]; prefix_len [B]; mask [B][R]
+    (uint64 or Python ints); positions [B][R]. Returns (out [B*R][Hq][d],
+    lse2 [B*R][Hq]), fp64.
+    """
+    rnd = round_bf16 if rope_out == "bf16" else (lambda a: a)
+    q = np.asarray(q)
+    B = len(prefix_len)
+    R = q.shape[0] // B
+    Hq, d = q.shape[1], q.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kc, vc = np.asarray(k_cache), np.asarray(v_cache)
+    out = np.zeros((B * R, Hq, d))
+    lse2 = np.zeros((B * R, Hq))
+    for b in range(B):
+        P = int(prefix_len[b])
+        pt = np.asarray(page_table[b], dtype=np.int64)
+        slots_all = prefix_slots(pt, P + W, page_size)
+        Kp = widen(kc[slots_all[:P]]).transpose(1, 0, 2)               # [Hkv][P][d]
+        Vp = widen(vc[slots_all[:P]]).transpose(1, 0, 2)
+        for r in range(R):
+            bits = int(mask[b][r])
+            win = [j for j in range(W) if (bits >> j) & 1]
+            Kw = widen(kc[slots_all[[P + j for j in win]]]).transpose(1, 0, 2) if win else np.zeros((Hkv, 0, d))
+            Vw = widen(vc[slots_all[[P + j for j in win]]]).transpose(1, 0, 2) if win else np.zeros((Hkv, 0, d))
+            qv = widen(q[b * R + r])
+            if not q_rotated:
+                qv = rnd(rope.rotate(qv, int(positions[b][r]), theta))
+            for kv in range(Hkv):
+                hs = slice(kv * g, (kv + 1) * g)
+                keys = np.concatenate([Kp[kv], Kw[kv]], axis=0)          # [P + |win|][d]
+                vals = np.concatenate([Vp[kv], Vw[kv]], axis=0)
+                if keys.shape[0] == 0:                                   # nothing visible (R22)
+                    out[b * R + r, hs] = 0.0
+                    lse2[b * R + r, hs] = -np.inf
+                    continue
+                s = (qv[hs] @ keys.T) * scale                            # [g][keys]
+                m = s.max(axis=1, keepdims=True)
+                e = np.exp(s - m)
+                Z = e.sum(axis=1)
+                out[b * R + r, hs] = (e @ vals) / Z[:, None]
+                lse2[b * R + r, hs] = (m[:, 0] + np.log(Z)) / LN2
+    return out, lse2

@@ -198,3 +198,26 @@ def test_argmax_mutations_caught(monkeypatch):
         for row, expect in ([[2.0, math.nan, 9.0, math.nan], 1], [[1.0, 7.0, 3.0, 7.0], 1]):
             caught = caught or _fails(PM.test_special_cases, row, expect)
         assert caught, bad.__name__
+
+
+def test_window_attention_mutations_caught(monkeypatch):
+    import oracle.attention as AT
+    from tests import test_oracle_window as PW2
+    real = AT.window_attention
+
+    def shifted_mask(q, kc, vc, pt, plen, mask, pos, W, *a, **k):      # bit j read as key j + 1
+        return real(q, kc, vc, pt, plen, [[(int(m) << 1) & ((1 << W) - 1) for m in row] for row in mask], pos, W,
+                    *a, **k)
+
+    def mask_ignored(q, kc, vc, pt, plen, mask, pos, W, *a, **k):      # every window key visible
+        return real(q, kc, vc, pt, plen, [[(1 << W) - 1 for _ in row] for row in mask], pos, W, *a, **k)
+
+    def position_by_row(q, kc, vc, pt, plen, mask, pos, W, *a, **k):   # the query at prefix + row index
+        return real(q, kc, vc, pt, plen, mask, [[int(plen[b]) + r for r in range(len(row))]
+                                                 for b, row in enumerate(pos)], W, *a, **k)
+
+    for bad in (shifted_mask, mask_ignored, position_by_row):
+        monkeypatch.setattr(AT, "window_attention", bad)
+        caught = _fails(PW2.test_lane_rows_equal_tree_rows)
+        caught = caught or _fails(PW2.test_equals_path_oracle_on_trees, [-1, 0, 0, 1, 2])
+        assert caught, bad.__name__
