@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-argmax", action="store_true", help="skip the target-argmax measurement")
+    ap.add_argument("--no-lanes", action="store_true", help="skip the draft-lane attention measurement")
     return ap.parse_args()
 
 
@@ -375,6 +376,8 @@ def run_ours(args, rank, world, local_rank):
         line["e2e"] = e2e
     if not args.no_argmax:
         line["target_argmax"] = time_target_argmax(inp, db, stream, flush, args, hbm)
+    if not args.no_lanes:
+        line["lane_attention"] = time_lane_attention(stream, flush, args, hbm, tf_sus, db.device)
     clocks = clk.summary()
     if clocks is not None:
         line["clocks"] = clocks
@@ -424,6 +427,60 @@ def time_target_argmax(inp, db, stream, flush, args, hbm):
     return {"us": us, "fused_walk_us": fused_us, "rows": rows, "vocab": w.vocab, "bytes": nbytes,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm},
             "argmax_matches_planted_target": ok, "reps": reps}
+
+
+LANE_WORKLOAD = "lanes_eagle2_p8192_k8_s7"
+
+
+def time_lane_attention(stream, flush, args, hbm, tf_sus, device):
+    """Draft-lane attention (dts_tree_window_attention with R = K lane rows
+    over the (S - 1) * K-key lane window) on the EAGLE-2 batch's drafting
+    shape, outside the headline step: CUDA-event time per call, L2 flushed
+    before each; roofline as for the verify attention (K/V of every prefix and
+    window key read once per KV head, plus q and out)."""
+    import torch
+    from draft_tree_speculative_gb300 import tree_window_attention, tree_window_attention_workspace
+    lw = synth.LANE_WORKLOADS[LANE_WORKLOAD]
+    li = synth.make_lane_inputs(lw)
+    B, R, W = lw.B, lw.R, lw.W
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    q, kc, vc = bf(li.q), bf(li.k_cache), bf(li.v_cache)
+    pt, plen, pos = t(li.layout.page_table), t(li.prefix_len), t(li.positions)
+    mask = t(li.mask.view(np.int64))
+    out = torch.empty((B * R, lw.Hq, lw.d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B * R, lw.Hq), dtype=torch.float32, device=device)
+    max_prefix = int(max(lw.prefix))
+    ws = torch.empty(tree_window_attention_workspace(B, R, W, lw.Hq, lw.Hkv, lw.d, max_prefix), dtype=torch.uint8,
+                     device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    reps = max(5, min(args.steps, 50))
+    call = lambda: tree_window_attention(q, kc, vc, pt, lw.page_size, plen, max_prefix, mask, pos, lw.rope_theta,
+                                         out, lse, ws, W, err=err, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            call()
+            b.record(stream)
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError(f"device reported error {int(err.item())} in the lane attention")
+    us = statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
+    P = np.asarray(lw.prefix, np.int64)
+    kv = 2 * lw.Hkv * lw.d * 2 * (int(P.sum()) + B * W)
+    rows = B * R * lw.Hq
+    nbytes = kv + 2 * rows * lw.d * 2 + rows * 4 + B * R * (8 + 4) + li.layout.page_table.size * 4 + B * 4
+    flops = 4 * R * lw.Hq * lw.d * int(P.sum())
+    t_hbm, t_mma = nbytes / (hbm * 1e9), flops / (tf_sus * 1e12)
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"workload": lw.name, "B": B, "R": R, "W": W, "prefix_len": int(P.max()), "us": us,
+            "rows_per_s": B * R / (us / 1e6), "bytes": nbytes, "flops": flops,
+            "roofline": {"bound": "hbm" if t_hbm >= t_mma else "tensor", "achieved": gbs, "peak": hbm,
+                         "unit": "GB/s", "frac": gbs / hbm}, "reps": reps}
 
 
 def run_reference(args):

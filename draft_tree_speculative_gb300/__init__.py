@@ -26,7 +26,7 @@ EXPORTED = (
     "dts_write_window_kv", "dts_tree_verify_attention_workspace", "dts_tree_verify_attention",
     "dts_verify_tree_greedy", "dts_compact_window_rows", "dts_compact_rows",
     "dts_tree_verify_attention_static_ws", "dts_target_argmax_workspace", "dts_target_argmax",
-    "dts_verify_tree_greedy_logits",
+    "dts_verify_tree_greedy_logits", "dts_tree_window_attention_workspace", "dts_tree_window_attention",
 )
 
 
@@ -52,6 +52,9 @@ _SIGS = {
     "dts_write_window_kv": (_I, [_P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _L, _F, _P, _P, _P, _P, _P]),
     "dts_tree_verify_attention_workspace": (_SZ, [_I, _I, _I, _I, _I, _L]),
     "dts_tree_verify_attention": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I, _F,
+                                       _P, _P, _P, _SZ, _P, _P]),
+    "dts_tree_window_attention_workspace": (_SZ, [_I, _I, _I, _I, _I, _I, _L]),
+    "dts_tree_window_attention": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I, _I, _F,
                                        _P, _P, _P, _SZ, _P, _P]),
     "dts_tree_verify_attention_static_ws": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I,
                                                  _F, _P, _P, _P, _P]),
@@ -210,6 +213,36 @@ def tree_verify_attention(q, k_cache, v_cache, page_table, page_size, prefix_len
         _ptr(prefix_len), int(max_prefix), _ptr(mask), _ptr(positions), float(rope_theta), B, N, Hq, Hkv, d,
         float(softmax_scale), _ptr(out), _ptr(lse2), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
     _raise(st, "tree_verify_attention")
+
+
+def tree_window_attention_workspace(B, R, W, Hq, Hkv, d, max_prefix) -> int:
+    return int(lib().dts_tree_window_attention_workspace(B, R, W, Hq, Hkv, d, int(max_prefix)))
+
+
+def tree_window_attention(q, k_cache, v_cache, page_table, page_size, prefix_len, max_prefix, mask, positions,
+                          rope_theta, out, lse2, workspace, W, softmax_scale=0.0, err=None, stream=None):
+    """R = q rows / B query rows per request over the prefix plus a W-key
+    masked window (draft lanes: R = K, W = (S - 1) * K)."""
+    torch = _torch()
+    BR, Hq, d = q.shape
+    B = prefix_len.shape[0]
+    if BR % B:
+        raise ValueError("q rows must be a multiple of B")
+    R = BR // B
+    Hkv = k_cache.shape[1]
+    _check(q, torch.bfloat16, (BR, Hq, d), "q")
+    _check(k_cache, torch.bfloat16, None, "k_cache")
+    _check(v_cache, torch.bfloat16, tuple(k_cache.shape), "v_cache")
+    _check(mask, _u64(), (B, R), "mask")
+    _check(positions, _i32(), (B, R), "positions")
+    _check(out, torch.bfloat16, (BR, Hq, d), "out")
+    _check(lse2, torch.float32, (BR, Hq), "lse2")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().dts_tree_window_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(page_table), page_table.shape[1], page_size,
+        _ptr(prefix_len), int(max_prefix), _ptr(mask), _ptr(positions), float(rope_theta), B, R, int(W), Hq, Hkv, d,
+        float(softmax_scale), _ptr(out), _ptr(lse2), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
+    _raise(st, "tree_window_attention")
 
 
 def tree_verify_attention_static_ws(q, k_cache, v_cache, page_table, page_size, prefix_len, max_prefix, mask,

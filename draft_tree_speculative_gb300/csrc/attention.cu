@@ -1,9 +1,12 @@
-// Tree-verify attention: every verify row attends the committed prefix plus
-// its own ancestors in the window.
+// Tree-window attention: every query row attends the committed prefix plus
+// the window keys its 64-bit mask selects. Verify: the N tree nodes are both
+// the rows and the window (R = W = N), the mask holds the row's ancestors.
+// Draft lanes: R = K lane rows over the (S - 1) * K-key lane window.
 //
 // [TS] "One tree attention": every row sees the committed prefix, and the
 // 64-bit ancestor mask applies only to the window keys; the prefix is where
-// the time goes at long context; results carry a base-2 log-sum-exp.
+// the time goes at long context; results carry a base-2 log-sum-exp; draft
+// lanes run the same with R = K over the lane window.
 // [AK] section one: row v equals Target(prefix + path(root -> v)).
 // [AK] section four: partial results over disjoint key sets merge by their
 // log-sum-exps, O = sum Z_k O_k / sum Z_k.
@@ -14,10 +17,10 @@
 //    in bf16 (the model dtype) in the workspace; writes NaN rows (and reports)
 //    for requests whose prefix length is out of range.
 //
-// 1. tree attention (tcgen05, persistent): the rows of a KV head are the N*g
-//    (node, query head) pairs; a "unit" is (request, KV head, pair of 128-row
-//    tiles), and its keys are the P prefix keys followed by the N window keys
-//    (the paged cache holds both), ceil((P + N)/128) key tiles. All units' key
+// 1. tree attention (tcgen05, persistent): the rows of a KV head are the R*g
+//    (row, query head) pairs; a "unit" is (request, KV head, pair of 128-row
+//    tiles), and its keys are the P prefix keys followed by the W window keys
+//    (the paged cache holds both), ceil((P + W)/128) key tiles. All units' key
 //    tiles form one flat sequence which the grid (one CTA per SM) splits into
 //    equal contiguous ranges, so every SM gets the same work whatever the
 //    prefix lengths. A CTA walks its range as segments (a unit's tiles inside
@@ -61,12 +64,12 @@ struct Plan {
 // Workspace: partial O [slots][slot_rows][d] fp32 | partial LSE
 // [slots][slot_rows] fp32 | tiles-before table [B+1] int64 | rotated queries
 // [B*N][Hq][d] bf16. A slot holds one unit's rows (at most two row tiles).
-Plan make_plan(int B, int N, int Hq, int Hkv, int d) {
+Plan make_plan(int B, int R, int Hq, int Hkv, int d) {
   Plan p;
   p.g = Hq / Hkv;
   p.npt = 128 / p.g;          // nodes per row tile
   p.rt = p.npt * p.g;         // rows per row tile (128 when g divides 128)
-  const int M = N * p.g;
+  const int M = R * p.g;
   p.n_pairs = (M + 2 * p.rt - 1) / (2 * p.rt);
   p.slot_rows = M < 2 * p.rt ? M : 2 * p.rt;
   p.units = static_cast<int64_t>(B) * Hkv * p.n_pairs;
@@ -75,7 +78,7 @@ Plan make_plan(int B, int N, int Hq, int Hkv, int d) {
   p.lse_off = align_up(p.o_off + p.slots * p.slot_rows * d * 4, 256);
   p.tb_off = align_up(p.lse_off + p.slots * p.slot_rows * 4, 256);
   p.q_off = align_up(p.tb_off + (static_cast<int64_t>(B) + 1) * 8, 256);
-  p.total = align_up(p.q_off + static_cast<int64_t>(B) * N * Hq * d * 2, 256);
+  p.total = align_up(p.q_off + static_cast<int64_t>(B) * R * Hq * d * 2, 256);
   return p;
 }
 
@@ -92,7 +95,7 @@ struct PrepArgs {
   float *lse2;
   int32_t *err;
   int64_t max_prefix, capacity;  // capacity: page-table rows x page size
-  int rows, N, Hq, heads_per_thread;      // rows = B*N nodes
+  int rows, R, W, Hq, heads_per_thread;   // rows = B*R query rows; W window keys per request
   dts::RopeFreqs freqs;
 };
 
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
   const int c = static_cast<int>(it % kChunks);
   const int hg = static_cast<int>((it / kChunks) % hgroups);
   const int64_t node = it / (static_cast<int64_t>(kChunks) * hgroups);
-  const int64_t b = node / a.N;
+  const int64_t b = node / a.R;
   // every load up front: prefix length, position and the group's query chunks
   const int P = a.prefix_len[b];
   const int pos = a.positions != nullptr ? a.positions[node] : 0;
@@ -123,9 +126,9 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
       x2[hh] = *reinterpret_cast<const uint4 *>(a.q + off + D / 2);
     }
   }
-  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.N > a.capacity) {
+  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.W > a.capacity) {
     // the attention pass skips this request: its rows read NaN
-    if (c == 0 && hg == 0 && node == b * a.N) dts::report(a.err, DTS_DEV_BAD_SLOT);
+    if (c == 0 && hg == 0 && node == b * a.R) dts::report(a.err, DTS_DEV_BAD_SLOT);
     const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
     for (int hh = 0; hh < a.heads_per_thread; ++hh) {
       const int h = hg * a.heads_per_thread + hh;
@@ -173,7 +176,7 @@ struct PrefixArgs {
   float *lse2;
   int32_t *err;
   int64_t num_slots, max_prefix;
-  int B, N, Hq, Hkv, g, M, rt, npt, n_pairs, slot_rows, max_pages, page_shift;
+  int B, R, W, Hq, Hkv, g, M, rt, npt, n_pairs, slot_rows, max_pages, page_shift;  // R rows, W window keys per request
   float scale_log2;
 };
 
@@ -192,12 +195,12 @@ struct PrefixShape {
 
 // Key tiles of one unit of request b: prefix and window keys together (0 for
 // a prefix length out of range; the prep kernel reports those).
-__device__ __forceinline__ int request_tiles(const int32_t *prefix_len, int b, int64_t max_prefix, int N,
+__device__ __forceinline__ int request_tiles(const int32_t *prefix_len, int b, int64_t max_prefix, int W,
                                              int max_pages, int page_shift) {
   const int P = prefix_len[b];
-  if (P < 0 || P > max_prefix || static_cast<int64_t>(P) + N > (static_cast<int64_t>(max_pages) << page_shift))
+  if (P < 0 || P > max_prefix || static_cast<int64_t>(P) + W > (static_cast<int64_t>(max_pages) << page_shift))
     return 0;
-  return (P + N + 127) >> 7;
+  return (P + W + 127) >> 7;
 }
 
 struct Segment {
@@ -215,7 +218,7 @@ struct SegmentWalker {
   __device__ void init(const PrefixArgs &a, int64_t x0, int64_t x_end) {
     b = 0;
     tb = 0;
-    nkt = a.B > 0 ? request_tiles(a.prefix_len, 0, a.max_prefix, a.N, a.max_pages, a.page_shift) : 0;
+    nkt = a.B > 0 ? request_tiles(a.prefix_len, 0, a.max_prefix, a.W, a.max_pages, a.page_shift) : 0;
     x = x0;
     x1 = x_end;
   }
@@ -225,7 +228,7 @@ struct SegmentWalker {
     while (x >= tb + nkt * per_req) {
       tb += nkt * per_req;
       ++b;
-      nkt = request_tiles(a.prefix_len, b, a.max_prefix, a.N, a.max_pages, a.page_shift);
+      nkt = request_tiles(a.prefix_len, b, a.max_prefix, a.W, a.max_pages, a.page_shift);
     }
     const int64_t off = x - tb;
     const int uir = static_cast<int>(off / nkt);
@@ -275,9 +278,9 @@ __device__ __forceinline__ uint32_t kind_phase(int use) {
 // key reported, and only the rows that see it turn NaN. Kept out of line so
 // that the MMA warp's issue loop keeps its registers.
 template <int D>
-__device__ __forceinline__ uint64_t clean_window_v(uint8_t *vt, int o, int N, int lane) {
+__device__ __forceinline__ uint64_t clean_window_v(uint8_t *vt, int o, int W, int lane) {
   constexpr uint32_t kBlockBytes = 128 * 128;
-  const int nvalid = min(128, N - o);  // rows holding prefix or window keys
+  const int nvalid = min(128, W - o);  // rows holding prefix or window keys
   for (int h = 0; h < D / 64; ++h) {
     uint4 *p = reinterpret_cast<uint4 *>(vt + h * kBlockBytes + nvalid * 128);
     const int n16 = (128 - nvalid) * 8;
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(384, 1)
     // total key tiles over all units
     int64_t part = 0;
     for (int b = lane; b < a.B; b += 32)
-      part += static_cast<int64_t>(request_tiles(a.prefix_len, b, a.max_prefix, a.N, a.max_pages, a.page_shift));
+      part += static_cast<int64_t>(request_tiles(a.prefix_len, b, a.max_prefix, a.W, a.max_pages, a.page_shift));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) range[0] = part * a.Hkv * a.n_pairs;
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(384, 1)
     int64_t acc = 0;
     for (int b = 0; b < a.B; ++b) {
       a.tiles_before[b] = acc;
-      acc += static_cast<int64_t>(request_tiles(a.prefix_len, b, a.max_prefix, a.N, a.max_pages, a.page_shift)) *
+      acc += static_cast<int64_t>(request_tiles(a.prefix_len, b, a.max_prefix, a.W, a.max_pages, a.page_shift)) *
              a.Hkv * a.n_pairs;
     }
     a.tiles_before[a.B] = acc;
@@ -455,13 +458,13 @@ __global__ void __launch_bounds__(384, 1)
             const int node0 = (sg.pair * 2 + t) * a.npt;
             for (int h = 0; h < D / 64; ++h)
               tma_load_4d(sQ_addr + t * kTileBytes + h * S::kBlockBytes, &tm_q, h * 64, 0, sg.hkv,
-                          sg.b * a.N + node0, q_full);
+                          sg.b * a.R + node0, q_full);
           }
         }
         ++segc;
         for (int lt = sg.lt0; lt < sg.lt1 && ok; ++lt) {
           const int kbase = lt * 128;
-          const int nvalid = min(128, sg.P + a.N - kbase);
+          const int nvalid = min(128, sg.P + a.W - kbase);
           int nbox = 0;
           for (int r = 0; r < boxes; ++r) nbox += box_slot(kbase, nvalid, r) >= 0 ? 1 : 0;
           for (int kv = 0; kv < 2; ++kv, ++use) {
@@ -622,7 +625,7 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           const int kbase = (sg.lt0 + j) * 128;
           if (kbase + 128 > sg.P)  // the window's tiles (and the unit's end)
-            seg_poison |= clean_window_v<D>(sKV + vslot * kTileBytes, kbase - sg.P, a.N, lane);
+            seg_poison |= clean_window_v<D>(sKV + vslot * kTileBytes, kbase - sg.P, a.W, lane);
           if (lane == 0) mbar_arrive(&vready[vslot]);
           __syncwarp();
         }
@@ -654,7 +657,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
     const float c = a.scale_log2;
-    const uint64_t node_bits = a.N < 64 ? (1ull << a.N) - 1ull : ~0ull;
+    const uint64_t node_bits = a.W < 64 ? (1ull << a.W) - 1ull : ~0ull;  // the window's keys
     int tcnt = 0, scnt = 0, wcnt = 0;
     bool ok = true;
     while (ok && walker.next(a, sg)) {
@@ -668,7 +671,7 @@ __global__ void __launch_bounds__(384, 1)
       const bool valid = warp_valid && r < a.rt && R < a.M;
       // the row's ancestor mask (bits >= N clear), read where a tile reaches the window
       auto row_mask = [&]() -> uint64_t {
-        return valid ? (a.mask[static_cast<int64_t>(sg.b) * a.N + R / a.g] & node_bits) : 0ull;
+        return valid ? (a.mask[static_cast<int64_t>(sg.b) * a.R + R / a.g] & node_bits) : 0ull;
       };
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nkt; ++j) {
@@ -773,7 +776,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t seg_poison = *poison;
       const bool poisoned = seg_poison != 0ull && (row_mask() & seg_poison) != 0ull;
       const int node = R / a.g;  // the row's tree node
-      const int64_t node_row = static_cast<int64_t>(sg.b) * a.N + node;
+      const int64_t node_row = static_cast<int64_t>(sg.b) * a.R + node;
       // l_run = 0: the row saw no key here (the part drops out of the merge);
       // a non-finite l_run (a non-finite score) stays non-finite
       const float inv_l = l_run == 0.f ? 0.f : 1.f / l_run;
@@ -856,7 +859,7 @@ struct MergeArgs {
   uint16_t *out;
   float *lse2;
   int64_t max_prefix, capacity;
-  int B, N, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;
+  int B, R, W, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;
   int owners32;  // every (tile index + 1) * groups fits in 32 bits
 };
 
@@ -900,8 +903,8 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   const int uir = static_cast<int>(unit - static_cast<uint32_t>(b) * per_req);
   const int hkv = uir / a.n_pairs, pair = uir - hkv * a.n_pairs;
   const int P = a.prefix_len[b];
-  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.N > a.capacity) return;  // NaN rows from prep
-  const int nkt = (P + a.N + 127) >> 7;
+  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.W > a.capacity) return;  // NaN rows from prep
+  const int nkt = (P + a.W + 127) >> 7;
   const Owners own{a.tiles_before[a.B], a.grid, a.owners32 != 0};
   const int64_t start = a.tiles_before[b] + static_cast<int64_t>(uir) * nkt;
   const int64_t c_first = own.of(start), c_last = own.of(start + nkt - 1);
@@ -988,7 +991,7 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
     const int R = pair * 2 * a.rt + prow;  // row of the KV head
     if (prow >= a.slot_rows || R >= a.M) continue;
     const int node = R / a.g;
-    const int64_t out_row = (static_cast<int64_t>(b) * a.N + node) * a.Hq + hkv * a.g + (R - node * a.g);
+    const int64_t out_row = (static_cast<int64_t>(b) * a.R + node) * a.Hq + hkv * a.g + (R - node * a.g);
     const float inv = den_i == 0.f ? 0.f : 1.f / den_i;  // (a NaN sum stays NaN)
     if constexpr (E == 4) {
       uint2 v;
@@ -1067,23 +1070,28 @@ int launch_prefix(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMa
 
 }  // namespace
 
-extern "C" size_t dts_tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d, int64_t max_prefix) {
-  if (B <= 0 || N < 1 || N > dts::kMaxNodes || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 128 ||
-      (d != 64 && d != 128) || max_prefix < 0)
+extern "C" size_t dts_tree_window_attention_workspace(int B, int R, int W, int Hq, int Hkv, int d,
+                                                      int64_t max_prefix) {
+  if (B <= 0 || R < 1 || R > dts::kMaxNodes || W < 1 || W > dts::kMaxNodes || Hkv < 1 || Hq < Hkv ||
+      Hq % Hkv != 0 || Hq / Hkv > 128 || (d != 64 && d != 128) || max_prefix < 0)
     return 0;
-  return static_cast<size_t>(make_plan(B, N, Hq, Hkv, d).total);
+  return static_cast<size_t>(make_plan(B, R, Hq, Hkv, d).total);
 }
 
-extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+extern "C" size_t dts_tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d, int64_t max_prefix) {
+  return dts_tree_window_attention_workspace(B, N, N, Hq, Hkv, d, max_prefix);
+}
+
+extern "C" int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                          int64_t num_slots, const int32_t *page_table, int max_pages,
                                          int page_size, const int32_t *prefix_len, int64_t max_prefix,
                                          const uint64_t *mask, const int32_t *positions, float rope_theta,
-                                         int B, int N, int Hq, int Hkv, int d, float softmax_scale,
+                                         int B, int R, int W, int Hq, int Hkv, int d, float softmax_scale,
                                          uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
                                          int32_t *err_dev, dts_stream_t stream) {
-  if (B < 0 || N < 1 || Hkv < 1 || Hq < 1 || max_pages < 1 || num_slots < 1 || max_prefix < 0)
+  if (B < 0 || R < 1 || W < 1 || Hkv < 1 || Hq < 1 || max_pages < 1 || num_slots < 1 || max_prefix < 0)
     return DTS_ERR_INVALID;
-  if (N > dts::kMaxNodes || (d != 64 && d != 128)) return DTS_ERR_UNSUPPORTED;
+  if (R > dts::kMaxNodes || W > dts::kMaxNodes || (d != 64 && d != 128)) return DTS_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return DTS_ERR_INVALID;
   if (Hq / Hkv > 128) return DTS_ERR_UNSUPPORTED;
   if (page_size < 8 || page_size > 4096 || (page_size & (page_size - 1)) != 0) return DTS_ERR_UNSUPPORTED;
@@ -1095,8 +1103,8 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
                        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out) |
                        reinterpret_cast<uintptr_t>(workspace);
   if (al & 15) return DTS_ERR_INVALID;
-  if (static_cast<int64_t>(B) * N * Hq >= (1ll << 31) / d) return DTS_ERR_UNSUPPORTED;
-  const Plan plan = make_plan(B, N, Hq, Hkv, d);
+  if (static_cast<int64_t>(B) * R * Hq >= (1ll << 31) / d) return DTS_ERR_UNSUPPORTED;
+  const Plan plan = make_plan(B, R, Hq, Hkv, d);
   if (workspace == nullptr || ws_bytes < static_cast<size_t>(plan.total)) return DTS_ERR_WORKSPACE;
   char *ws = static_cast<char *>(workspace);
   float *o_part = reinterpret_cast<float *>(ws + plan.o_off);
@@ -1120,12 +1128,13 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
     ra.err = err_dev;
     ra.max_prefix = max_prefix;
     ra.capacity = static_cast<int64_t>(max_pages) << page_shift;
-    ra.rows = B * N;
-    ra.N = N;
+    ra.rows = B * R;
+    ra.R = R;
+    ra.W = W;
     ra.Hq = Hq;
     ra.heads_per_thread = (Hq % 4 == 0) ? 4 : (Hq % 2 == 0) ? 2 : 1;
     if (positions != nullptr) dts_host::make_rope_freqs(rope_theta, d, &ra.freqs);
-    const int64_t items = static_cast<int64_t>(B) * N * (Hq / ra.heads_per_thread) * (d / 16);
+    const int64_t items = static_cast<int64_t>(B) * R * (Hq / ra.heads_per_thread) * (d / 16);
     const int blocks = static_cast<int>((items + 255) / 256);
     if (d == 128) attn_prep_kernel<128><<<blocks, 256, 0, s>>>(ra);
     else attn_prep_kernel<64><<<blocks, 256, 0, s>>>(ra);
@@ -1139,7 +1148,7 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   CUtensorMap tk, tv, tq;
   const int rpb = page_size < 128 ? page_size : 128;
   if (!make_cache_map(&tk, k_cache, d, Hkv, num_slots, rpb) || !make_cache_map(&tv, v_cache, d, Hkv, num_slots, rpb) ||
-      !make_q_map(&tq, q_eff, d, g, Hkv, static_cast<int64_t>(B) * N, plan.npt))
+      !make_q_map(&tq, q_eff, d, g, Hkv, static_cast<int64_t>(B) * R, plan.npt))
     return DTS_ERR_CUDA;
   PrefixArgs pa;
   pa.page_table = page_table;
@@ -1154,11 +1163,12 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   pa.num_slots = num_slots;
   pa.max_prefix = max_prefix;
   pa.B = B;
-  pa.N = N;
+  pa.R = R;
+  pa.W = W;
   pa.Hq = Hq;
   pa.Hkv = Hkv;
   pa.g = g;
-  pa.M = N * g;
+  pa.M = R * g;
   pa.rt = plan.rt;
   pa.npt = plan.npt;
   pa.n_pairs = plan.n_pairs;
@@ -1180,18 +1190,19 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   ma.max_prefix = max_prefix;
   ma.capacity = static_cast<int64_t>(max_pages) << page_shift;
   ma.B = B;
-  ma.N = N;
+  ma.R = R;
+  ma.W = W;
   ma.Hq = Hq;
   ma.Hkv = Hkv;
   ma.g = g;
-  ma.M = N * g;
+  ma.M = R * g;
   ma.rt = plan.rt;
   ma.n_pairs = plan.n_pairs;
   ma.slot_rows = plan.slot_rows;
   ma.grid = grid;
   {
     // the largest possible tile total, times the groups, against 2^32
-    const int64_t max_tiles = static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + N + 127) / 128);
+    const int64_t max_tiles = static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + W + 127) / 128);
     ma.owners32 = static_cast<double>(max_tiles + 1) * grid < 4294967296.0 ? 1 : 0;
   }
   const int64_t warps = plan.units * ((plan.slot_rows + 7) / 8);
@@ -1199,6 +1210,19 @@ extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_ca
   if (d == 128) tree_merge_kernel<128><<<blocks, 256, 0, s>>>(ma);
   else tree_merge_kernel<64><<<blocks, 256, 0, s>>>(ma);
   return dts_host::launch_status();
+}
+
+extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                         int64_t num_slots, const int32_t *page_table, int max_pages,
+                                         int page_size, const int32_t *prefix_len, int64_t max_prefix,
+                                         const uint64_t *mask, const int32_t *positions, float rope_theta,
+                                         int B, int N, int Hq, int Hkv, int d, float softmax_scale,
+                                         uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
+                                         int32_t *err_dev, dts_stream_t stream) {
+  // verify: the N tree nodes are both the query rows and the window keys
+  return dts_tree_window_attention(q, k_cache, v_cache, num_slots, page_table, max_pages, page_size, prefix_len,
+                                   max_prefix, mask, positions, rope_theta, B, N, N, Hq, Hkv, d, softmax_scale, out,
+                                   lse2, workspace, ws_bytes, err_dev, stream);
 }
 
 // ============================================================================

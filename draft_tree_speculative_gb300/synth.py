@@ -393,6 +393,92 @@ def target_logits(w: Workload, target_argmax: np.ndarray) -> np.ndarray:
     return x
 
 
+# ----------------------------------------------------------------------------
+# Draft-lane attention inputs (drafter side: lane ancestry and lane masks)
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class LaneWorkload:
+    """K lane rows per request at drafting step `step` (1 <= step <= S - 1;
+    0 means the last, S - 1) over the (S - 1) * K-key lane window of the
+    draft cache; window key (s - 1) * K + r is the key lane r wrote at step s."""
+    name: str
+    index: int
+    B: int
+    K: int
+    S: int
+    Hq: int
+    Hkv: int
+    d: int
+    prefix: Sequence[int]
+    step: int = 0
+    page_size: int = PAGE_SIZE
+    rope_theta: float = ROPE_THETA
+
+    @property
+    def W(self) -> int:
+        return (self.S - 1) * self.K
+
+    @property
+    def R(self) -> int:
+        return self.K
+
+
+LANE_WORKLOADS = {
+    # the EAGLE-2 batch's drafting: topk 8 lanes, 6 drafting steps (S = 7), the
+    # draft head with the target's attention shape, over its 8192-token frontier
+    "lanes_eagle2_p8192_k8_s7": LaneWorkload("lanes_eagle2_p8192_k8_s7", 10, B=32, K=8, S=7, Hq=32, Hkv=8, d=128,
+                                             prefix=[8192] * 32),
+}
+
+
+@dataclasses.dataclass
+class LaneInputs:
+    lw: LaneWorkload
+    mask: np.ndarray        # uint64 [B][K]: bit j = window key j is an ancestor of (or is) the lane's token
+    positions: np.ndarray   # int32 [B][K]: the lane tokens' positions
+    layout: PagedLayout
+    q: np.ndarray           # bf16 bits [B*K][Hq][d] (not rotated)
+    k_cache: np.ndarray     # bf16 bits [num_slots][Hkv][d] (all keys already rotated)
+    v_cache: np.ndarray
+
+    @property
+    def prefix_len(self) -> np.ndarray:
+        return self.layout.prefix_len
+
+
+def make_lane_inputs(lw: LaneWorkload) -> LaneInputs:
+    """Seeded lane inputs. The drafter's beam keeps K lanes per step; lane r of
+    step s >= 2 descends from a lane of step s - 1 drawn uniformly (several
+    lanes may share a parent), and a lane's mask holds its own key's bit and
+    its ancestors' (one per earlier step)."""
+    s = streams(lw.index)
+    B, K, W = lw.B, lw.K, lw.W
+    step = lw.step or lw.S - 1
+    rng = s["tree"]
+    masks = np.zeros((B, K), np.uint64)
+    for b in range(B):
+        prev = [0] * K
+        for st in range(1, step + 1):
+            cur = []
+            for r in range(K):
+                m = 1 << ((st - 1) * K + r)
+                if st >= 2:
+                    m |= prev[int(rng.integers(0, K))]
+                cur.append(m)
+            prev = cur
+        masks[b] = np.array(prev, dtype=np.uint64)
+    plen = np.array(lw.prefix, np.int32)
+    w = Workload(lw.name, lw.index, B=B, Hq=lw.Hq, Hkv=lw.Hkv, d=lw.d, N=W, prefix=list(lw.prefix), tree="lanes",
+                 page_size=lw.page_size, rope_theta=lw.rope_theta)
+    lay = make_layout(w, plen, s["pages"])
+    positions = (plen[:, None] + step - 1 + np.zeros((1, K), np.int32)).astype(np.int32)
+    q = normal_bf16(s["q"], (B * K, lw.Hq, lw.d))
+    k_cache = normal_bf16(s["k_cache"], (lay.num_slots, lw.Hkv, lw.d))
+    v_cache = normal_bf16(s["v_cache"], (lay.num_slots, lw.Hkv, lw.d))
+    return LaneInputs(lw, masks, positions, lay, q, k_cache, v_cache)
+
+
 def fp8_window_rows(w: Workload, n_buffers: int, row_bytes: int) -> np.ndarray:
     """Random bytes for the window slots of each fp8 K/V buffer: uint8 [L][B*N][row_bytes]."""
     rng = streams(w.index)["fp8"]

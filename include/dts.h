@@ -10,6 +10,8 @@
  *   dts_write_window_kv         RoPE'd window K and V into the paged cache
  *   dts_tree_verify_attention   every row attends the committed prefix plus
  *                               its own ancestors; out + base-2 LSE
+ *   dts_tree_window_attention   the same over R rows and a W-key masked window
+ *                               (draft lanes: R = K rows, W = (S - 1) * K keys)
  *   dts_verify_tree_greedy      greedy walk -> accept_len, packed path, tokens
  *   dts_target_argmax           the target's argmax per verify row (and
  *   dts_verify_tree_greedy_logits  that argmax fed straight into the walk)
@@ -185,6 +187,53 @@ int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache,
                               float softmax_scale, uint16_t *out, float *lse2,
                               void *workspace, size_t ws_bytes, int32_t *err_dev,
                               dts_stream_t stream);
+
+/*
+ * dts_tree_window_attention_workspace - bytes of device workspace that
+ * dts_tree_window_attention needs (the same plan as
+ * dts_tree_verify_attention_workspace with R query rows per request; W does
+ * not enter it), or 0 if the shape is unsupported. Host-only.
+ */
+size_t dts_tree_window_attention_workspace(int B, int R, int W, int Hq, int Hkv, int d,
+                                           int64_t max_prefix);
+
+/*
+ * dts_tree_window_attention - attention of R query rows per request over the
+ * committed prefix plus a masked window of W keys (the general form of
+ * dts_tree_verify_attention, which is this call with R = W = N).
+ *
+ * Defined by [TS] "One tree attention": every row sees the committed prefix,
+ * and the 64-bit mask applies only to the last W keys; verify runs it with
+ * R = W = N, draft lanes with R = K rows over the (S - 1) * K-key lane window.
+ * [TS] "Draft lanes write the draft cache like any draft step": every lane row
+ * sees the accepted frontier and, inside the window, only its ancestors'
+ * slots (the lane mask); step s lane r writes slot frontier + (s - 1) * K + r.
+ *
+ *   q          bf16 [B*R][Hq][d]       row r of request b at b*R + r; rotated
+ *                                      here at positions[b][r] unless
+ *                                      positions is NULL
+ *   k_cache, v_cache bf16 [num_slots][Hkv][d]  paged cache holding the prefix
+ *                                      and the window, all keys already rotated
+ *                                      at their own positions
+ *   page_table, prefix_len, max_prefix as for dts_tree_verify_attention;
+ *                                      window key j is at logical position P_b + j
+ *   mask       u64 [B][R]              bit j: row r sees window key j (j < W)
+ *   positions  int32 [B][R] or NULL
+ *   out        bf16 [B*R][Hq][d]; lse2 fp32 [B*R][Hq]   outputs
+ *   workspace  device, >= dts_tree_window_attention_workspace(...) bytes
+ *
+ * 1 <= R <= 64 and 1 <= W <= 64; every other constraint, output rule and
+ * error is as for dts_tree_verify_attention (with W in place of N for the
+ * window and R for the rows).
+ */
+int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_cache,
+                              const uint16_t *v_cache, int64_t num_slots,
+                              const int32_t *page_table, int max_pages, int page_size,
+                              const int32_t *prefix_len, int64_t max_prefix,
+                              const uint64_t *mask, const int32_t *positions, float rope_theta,
+                              int B, int R, int W, int Hq, int Hkv, int d, float softmax_scale,
+                              uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
+                              int32_t *err_dev, dts_stream_t stream);
 
 /*
  * dts_tree_verify_attention_static_ws - dts_tree_verify_attention without a
