@@ -24,6 +24,7 @@ Modules: ``tree`` (validation, ancestor mask, positions, links), ``rope``,
 ``attention`` (per-path literal attention), ``walk`` (greedy verification),
 ``compact`` (KV-row / hidden-row / position compaction), ``merge`` (the
 log-sum-exp combine rule), ``argmax`` (the target's argmax per verify row and
-the walk fed by it).
+the walk fed by it), ``sampling`` (Gumbel-max draws keyed by position and the
+walk over them).
 """
-from . import tree, rope, attention, walk, compact, merge, argmax  # noqa: F401
+from . import tree, rope, attention, walk, compact, merge, argmax, sampling  # noqa: F401

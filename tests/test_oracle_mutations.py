@@ -221,3 +221,37 @@ def test_window_attention_mutations_caught(monkeypatch):
         caught = _fails(PW2.test_lane_rows_equal_tree_rows)
         caught = caught or _fails(PW2.test_equals_path_oracle_on_trees, [-1, 0, 0, 1, 2])
         assert caught, bad.__name__
+
+
+def test_sampling_mutations_caught(monkeypatch):
+    import oracle.sampling as SM
+    from tests import test_oracle_sampling as PS
+    real_scores, real_gumbel, real_draws = SM.sampled_scores, SM.gumbel_f32, SM.sampled_draws
+
+    def draws_pos_without_plus_one(logits, vc, depth, temperature, seed):   # the node's own position
+        depth = np.asarray(depth)
+        return real_draws(logits, np.asarray(vc) - 1, depth, temperature, seed)
+
+    def draws_keyed_by_row(logits, vc, depth, temperature, seed):
+        depth = np.asarray(depth)
+        B, N = depth.shape
+        rows = np.tile(np.arange(N), (B, 1))
+        return real_draws(logits, np.zeros(B, np.int64), rows, temperature, seed)
+
+    def scores_ignore_temperature(x, temperature, seed, pos):
+        return real_scores(x, 1.0 if temperature > 0 else temperature, seed, pos)
+
+    def gumbel_log2(seed, pos, vocab):
+        g = real_gumbel(seed, pos, vocab).astype(np.float64)
+        # the same uniforms through -log2(-log2(u)) instead of -ln(-ln(u))
+        u = np.exp(-np.exp(-g))
+        return (-np.log2(-np.log2(u))).astype(np.float32)
+
+    cases = [("sampled_draws", draws_pos_without_plus_one, PS.test_chain_accepts_plain_decoding_draws, ()),
+             ("sampled_draws", draws_keyed_by_row, PS.test_keyed_by_position_not_row, ()),
+             ("sampled_scores", scores_ignore_temperature, PS.test_draws_follow_softmax, (0.7,)),
+             ("gumbel_f32", gumbel_log2, PS.test_draws_follow_softmax, (1.0,))]
+    for name, bad, pin, args in cases:
+        monkeypatch.setattr(SM, name, bad)
+        assert _fails(pin, *args), bad.__name__
+        monkeypatch.undo()
