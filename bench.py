@@ -395,7 +395,8 @@ def time_target_argmax(inp, db, stream, flush, args, hbm):
     CUDA-event time of the argmax call alone and of the fused call, L2 flushed
     before each; the argmax streams the logits once, so its roofline is HBM."""
     import torch
-    from draft_tree_speculative_gb300 import target_argmax, target_argmax_workspace, verify_tree_greedy_logits
+    from draft_tree_speculative_gb300 import (sample_draws, target_argmax, target_argmax_workspace,
+                                              verify_tree_greedy_logits, verify_tree_sampled)
     w = inp.w
     rows = w.B * w.N
     logits = torch.from_numpy(synth.target_logits(w, inp.target_argmax)).to(db.device)
@@ -424,9 +425,21 @@ def time_target_argmax(inp, db, stream, flush, args, hbm):
     ok = bool((arg.cpu().numpy() == inp.target_argmax).all())
     nbytes = rows * w.vocab * 4
     gbs = nbytes / (us / 1e6) / 1e9
+    # sampled verify (Gumbel-max keyed by position) over the same logits, T = 1
+    temp = torch.ones(w.B, dtype=torch.float32, device=db.device)
+    seed = torch.arange(w.B, dtype=torch.int64, device=db.device) * 7919 + 1
+    draws = torch.empty((w.B, w.N), dtype=torch.int32, device=db.device)
+    samp_us = timed(lambda: sample_draws(logits, db.vc, db.depth, temp, seed, draws, ws, stream=stream))
+    samp_walk_us = timed(lambda: verify_tree_sampled(db.draft, logits, db.vc, db.depth, temp, seed, draws,
+                                                     db.accept_len, db.accepted_path, db.accepted_tokens, ws,
+                                                     parents=db.parents, err=db.err, stream=stream))
+    check_device_error(db, "the sampled draws and walk")
+    elems = rows * w.vocab
     return {"us": us, "fused_walk_us": fused_us, "rows": rows, "vocab": w.vocab, "bytes": nbytes,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm},
-            "argmax_matches_planted_target": ok, "reps": reps}
+            "argmax_matches_planted_target": ok, "reps": reps,
+            "sampled": {"us": samp_us, "fused_walk_us": samp_walk_us, "logits_per_s": elems / (samp_us / 1e6),
+                        "hbm_gbs": nbytes / (samp_us / 1e6) / 1e9, "hbm_frac": nbytes / (samp_us / 1e6) / 1e9 / hbm}}
 
 
 LANE_WORKLOAD = "lanes_eagle2_p8192_k8_s7"

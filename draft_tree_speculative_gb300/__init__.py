@@ -27,6 +27,7 @@ EXPORTED = (
     "dts_verify_tree_greedy", "dts_compact_window_rows", "dts_compact_rows",
     "dts_tree_verify_attention_static_ws", "dts_target_argmax_workspace", "dts_target_argmax",
     "dts_verify_tree_greedy_logits", "dts_tree_window_attention_workspace", "dts_tree_window_attention",
+    "dts_sample_draws", "dts_verify_tree_sampled",
 )
 
 
@@ -60,6 +61,9 @@ _SIGS = {
                                                  _F, _P, _P, _P, _P]),
     "dts_verify_tree_greedy": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "dts_target_argmax_workspace": (_SZ, [_L, _I]),
+    "dts_sample_draws": (_I, [_P, _I, _L, _P, _P, _P, _P, _I, _I, _P, _P, _SZ, _P]),
+    "dts_verify_tree_sampled": (_I, [_P, _P, _I, _L, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _SZ, _P,
+                                     _P]),
     "dts_target_argmax": (_I, [_P, _L, _I, _L, _P, _P, _SZ, _P]),
     "dts_verify_tree_greedy_logits": (_I, [_P, _P, _I, _L, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "dts_compact_window_rows": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P]),
@@ -328,6 +332,51 @@ def verify_tree_greedy_logits(draft_tokens, logits, target_argmax, accept_len, a
                                              _ptr(accepted_path), _ptr(accepted_tokens), _ptr(workspace), ws_bytes,
                                              _ptr(err), _stream(stream))
     _raise(st, "verify_tree_greedy_logits")
+
+
+def sample_draws(logits, vc, depth, temperature, seed, draws, workspace, stream=None):
+    """draws [B][N] <- Gumbel-max draws of logits [B*N][vocab] keyed by
+    (seed[b], vc[b] + depth[b][i] + 1); temperature float32 [B], seed int64/uint64 [B]."""
+    torch = _torch()
+    B, N = depth.shape
+    p, rows, vocab, stride = _logits(logits)
+    if rows != B * N:
+        raise ValueError("logits must have B*N rows")
+    _check(vc, _i32(), (B,), "vc")
+    _check(depth, _i32(), (B, N), "depth")
+    _check(temperature, torch.float32, (B,), "temperature")
+    _check(seed, _u64(), (B,), "seed")
+    _check(draws, _i32(), (B, N), "draws")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().dts_sample_draws(p, vocab, stride, _ptr(vc), _ptr(depth), _ptr(temperature), _ptr(seed), B, N,
+                                _ptr(draws), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise(st, "sample_draws")
+
+
+def verify_tree_sampled(draft_tokens, logits, vc, depth, temperature, seed, draws, accept_len, accepted_path,
+                        accepted_tokens, workspace, parents=None, next_token=None, next_sibling=None, err=None,
+                        stream=None):
+    """Sampled draws (sample_draws), then the greedy walk over them."""
+    torch = _torch()
+    B, N = draft_tokens.shape
+    p, rows, vocab, stride = _logits(logits)
+    if rows != B * N:
+        raise ValueError("logits must have B*N rows")
+    i32 = _i32()
+    for name, t in (("draft_tokens", draft_tokens), ("depth", depth), ("draws", draws), ("parents", parents),
+                    ("next_token", next_token), ("next_sibling", next_sibling),
+                    ("accepted_path", accepted_path), ("accepted_tokens", accepted_tokens)):
+        _check(t, i32, (B, N), name)
+    _check(vc, i32, (B,), "vc")
+    _check(accept_len, i32, (B,), "accept_len")
+    _check(temperature, torch.float32, (B,), "temperature")
+    _check(seed, _u64(), (B,), "seed")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().dts_verify_tree_sampled(_ptr(draft_tokens), p, vocab, stride, _ptr(vc), _ptr(depth), _ptr(temperature),
+                                       _ptr(seed), _ptr(parents), _ptr(next_token), _ptr(next_sibling), B, N,
+                                       _ptr(draws), _ptr(accept_len), _ptr(accepted_path), _ptr(accepted_tokens),
+                                       _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
+    _raise(st, "verify_tree_sampled")
 
 
 def make_kv_table(entries: Sequence, device="cuda"):

@@ -15,6 +15,8 @@
  *   dts_verify_tree_greedy      greedy walk -> accept_len, packed path, tokens
  *   dts_target_argmax           the target's argmax per verify row (and
  *   dts_verify_tree_greedy_logits  that argmax fed straight into the walk)
+ *   dts_sample_draws            sampled draws, Gumbel-max keyed by position (and
+ *   dts_verify_tree_sampled     the walk over them)
  *   dts_compact_window_rows     the path's KV rows -> the window's front slots
  *   dts_compact_rows            the path's hidden rows -> the front; positions
  *                               back to vc + i
@@ -341,6 +343,53 @@ int dts_verify_tree_greedy_logits(const int32_t *draft_tokens, const float *logi
                                   int32_t *accepted_path, int32_t *accepted_tokens,
                                   void *workspace, size_t ws_bytes, int32_t *err_dev,
                                   dts_stream_t stream);
+
+/*
+ * dts_sample_draws - the sampled target token of every verify row, drawn by
+ * Gumbel-max keyed by position.
+ *
+ * Defined by [TS] "Sampled verify keys noise by position": a row's target
+ * token is drawn by Gumbel-max keyed by (seed, position); for a tree the key
+ * is the position the node predicts, vc + depth + 1, never its row, so the
+ * token accepted at every position is the one plain decoding samples there.
+ *
+ *   logits       float [B*N][row_stride]  row b*N+i for node i of request b
+ *   vc           int32 [B]     the pre-forward frontier (committed prefix length)
+ *   depth        int32 [B][N]  node depths
+ *   temperature  float [B]     T_b; T_b <= 0 or not finite: the plain argmax
+ *   seed         uint64 [B]    the request's sampling seed
+ *   draws        int32 [B][N]  out: argmax_v x_v * (1/T_b) + G(seed_b, vc_b + depth + 1, v)
+ *   workspace    dts_target_argmax_workspace(B*N, vocab) bytes, as for
+ *                dts_target_argmax
+ *
+ * G is fixed exactly, so that a draw is reproducible bit for bit: Philox4x32-10
+ * (Salmon, Moraes, Dror and Shaw, SC 2011) with key (seed low word, seed high
+ * word) and counter (v / 4, position, 0, 0), word v % 4 for vocabulary entry
+ * v; u = (2 (word >> 9) + 1) 2^-24; G = -ln(-ln u), with ln and the scaling
+ * evaluated in float32, one rounding per operation, by the series stated in
+ * csrc/argmax.cu. Ties and NaN follow dts_target_argmax. Errors as for
+ * dts_target_argmax; DTS_ERR_INVALID for a NULL vc, depth, temperature or seed.
+ */
+int dts_sample_draws(const float *logits, int vocab, int64_t row_stride, const int32_t *vc,
+                     const int32_t *depth, const float *temperature, const uint64_t *seed, int B,
+                     int N, int32_t *draws, void *workspace, size_t ws_bytes,
+                     dts_stream_t stream);
+
+/*
+ * dts_verify_tree_sampled - dts_sample_draws, then dts_verify_tree_greedy over
+ * the draws ([TS] "Sampled verify keys noise by position": acceptance is the
+ * greedy tree walk over those draws, a child accepted when it equals its
+ * parent's draw), in one call on `stream`. draws [B][N] is an output; every
+ * other argument is as for those two calls.
+ */
+int dts_verify_tree_sampled(const int32_t *draft_tokens, const float *logits, int vocab,
+                            int64_t row_stride, const int32_t *vc, const int32_t *depth,
+                            const float *temperature, const uint64_t *seed,
+                            const int32_t *parents, const int32_t *next_token,
+                            const int32_t *next_sibling, int B, int N, int32_t *draws,
+                            int32_t *accept_len, int32_t *accepted_path,
+                            int32_t *accepted_tokens, void *workspace, size_t ws_bytes,
+                            int32_t *err_dev, dts_stream_t stream);
 
 /*
  * One K or V buffer of one layer (an entry of a cache group's address table).
