@@ -105,6 +105,30 @@ def recorded_traffic(workload):
     return e.get("bytes_per_call")
 
 
+def load_sm_max_mhz():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f).get("sm_max_mhz", 2070.0))
+    return 2070.0
+
+
+def recorded_instructions(name, workload):
+    """Warp instructions per call of a kernel from the committed ncu summary,
+    if it was taken on the current source for this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "instruction_counts.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        e = json.load(f).get(name)
+    src = os.path.join(ROOT, "draft_tree_speculative_gb300", "csrc", "argmax.cu")
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if not e or e.get("source_hash") != h or e.get("workload") != workload:
+        return None
+    return e.get("warp_instructions_per_call")
+
+
 def check_device_error(db, when):
     from draft_tree_speculative_gb300 import device_error_string
     code = int(db.err.item())
@@ -435,11 +459,22 @@ def time_target_argmax(inp, db, stream, flush, args, hbm):
                                                      parents=db.parents, err=db.err, stream=stream))
     check_device_error(db, "the sampled draws and walk")
     elems = rows * w.vocab
+    # the sampled draws are bound by instruction issue: achieved warp
+    # instructions per second (the profiled count per call, while the source
+    # is unchanged) against 4 per SM per cycle at the maximum SM clock
+    sm_count = torch.cuda.get_device_properties(db.device).multi_processor_count
+    alu_peak = sm_count * 4 * load_sm_max_mhz() * 1e6
+    inst = recorded_instructions("sampled_draws", w.name)
+    alu = None
+    if inst is not None:
+        alu = {"bound": "alu", "achieved": inst / (samp_us / 1e6), "peak": alu_peak, "unit": "warp-inst/s",
+               "frac": inst / (samp_us / 1e6) / alu_peak, "warp_instructions_per_call": inst}
     return {"us": us, "fused_walk_us": fused_us, "rows": rows, "vocab": w.vocab, "bytes": nbytes,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm},
             "argmax_matches_planted_target": ok, "reps": reps,
             "sampled": {"us": samp_us, "fused_walk_us": samp_walk_us, "logits_per_s": elems / (samp_us / 1e6),
-                        "hbm_gbs": nbytes / (samp_us / 1e6) / 1e9, "hbm_frac": nbytes / (samp_us / 1e6) / 1e9 / hbm}}
+                        "hbm_gbs": nbytes / (samp_us / 1e6) / 1e9, "hbm_frac": nbytes / (samp_us / 1e6) / 1e9 / hbm,
+                        "roofline": alu}}
 
 
 LANE_WORKLOAD = "lanes_eagle2_p8192_k8_s7"

@@ -180,7 +180,7 @@ struct Best {
 // kVec4: the row starts on a 16-byte boundary (logits aligned, row stride a
 // multiple of 4), so whole float4 words inside the row are read as such.
 template <bool kVec4, bool kSample>
-__global__ void __launch_bounds__(kThreads) argmax_chunk_kernel(const float *logits, int64_t row_stride, int vocab,
+__global__ void __launch_bounds__(kThreads, kSample ? 6 : 1) argmax_chunk_kernel(const float *logits, int64_t row_stride, int vocab,
                                                                 int chunks, uint64_t *best, Sampler sp) {
   const int64_t blk = blockIdx.x;
   const int64_t row = blk / chunks;
@@ -212,12 +212,19 @@ __global__ void __launch_bounds__(kThreads) argmax_chunk_kernel(const float *log
     else bt.see(x, e);
   };
   if (kVec4 && hi - lo == kChunk) {
-    // a whole chunk: every load issued first, no bounds to test
-    float4 v[kVec];
+    // a whole chunk, no bounds to test. The plain argmax is bound by HBM: every
+    // load is issued first. The sampled scores are bound by arithmetic: four
+    // loads at a time keep the registers (and so the warps per SM) for it.
+    constexpr int kDepth = kSample ? 4 : kVec;
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) v[k] = __ldcs(reinterpret_cast<const float4 *>(src + lo) + k * kThreads + tid);
+    for (int k0 = 0; k0 < kVec; k0 += kDepth) {
+      float4 v[kDepth];
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) see4(v[k], lo + (k * kThreads + tid) * 4);
+      for (int k = 0; k < kDepth; ++k)
+        v[k] = __ldcs(reinterpret_cast<const float4 *>(src + lo) + (k0 + k) * kThreads + tid);
+#pragma unroll
+      for (int k = 0; k < kDepth; ++k) see4(v[k], lo + ((k0 + k) * kThreads + tid) * 4);
+    }
   } else if (kVec4) {
     // the row's last chunk: whole float4 words, then the ragged end
     for (int e = lo + tid * 4; e < hi; e += kThreads * 4) {
