@@ -355,32 +355,62 @@ def run_ours(args, rank, world, local_rank):
     roof["roofline_us"] = max(t_hbm, t_mma) * 1e6
     roof["attention_us"] = attn_ms * 1e3
 
-    # end to end through the public API: pinned host inputs in, result out
+    # end to end through the public API: pinned host inputs in, result out.
+    # A serving loop overlaps the next step's upload with this step's compute:
+    # the inputs are double-buffered on the device, each step's upload runs on
+    # a copy stream once the step that last used its buffer has finished, and
+    # the step waits for its upload. Every step still copies its inputs from
+    # pinned host memory and reads its result back inside the timed region.
     e2e = None
     if not args.no_e2e:
-        host = {k: getattr(db, k).cpu().pin_memory() for k in
-                ("q", "k_new", "v_new", "parents", "depth", "vc", "draft", "target_argmax")}
+        in_names = ("q", "k_new", "v_new", "parents", "depth", "vc", "draft", "target_argmax")
+        host = {k: getattr(db, k).cpu().pin_memory() for k in in_names}
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        out_alen = torch.empty_like(db.accept_len, device="cpu").pin_memory()
-        out_tok = torch.empty_like(db.accepted_tokens, device="cpu").pin_memory()
-        d2h = out_alen.numel() * 4 + out_tok.numel() * 4
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        with torch.cuda.stream(stream):
-            for s in range(args.warmup + args.steps):
-                flush.fill_(1)
-                if s >= args.warmup:
-                    ev[s - args.warmup][0].record(stream)
-                for k, t in host.items():
-                    getattr(db, k).copy_(t, non_blocking=True)
+        bufs = [{k: getattr(db, k) for k in in_names}, {k: torch.empty_like(getattr(db, k)) for k in in_names}]
+        outs = [(torch.empty_like(db.accept_len, device="cpu").pin_memory(),
+                 torch.empty_like(db.accepted_tokens, device="cpu").pin_memory()) for _ in range(2)]
+        d2h = outs[0][0].numel() * 4 + outs[0][1].numel() * 4
+        copy_stream = torch.cuda.Stream(device=dev)
+        ready = [torch.cuda.Event() for _ in range(2)]
+        freed = [None, None]
+
+        def pipelined(nsteps):
+            for st in range(nsteps):
+                i = st % 2
+                with torch.cuda.stream(copy_stream):
+                    if freed[i] is not None:
+                        copy_stream.wait_event(freed[i])
+                    for k, t in host.items():
+                        bufs[i][k].copy_(t, non_blocking=True)
+                    ready[i].record(copy_stream)
+                stream.wait_event(ready[i])
+                for k in in_names:
+                    setattr(db, k, bufs[i][k])
+                db.prefix_len = db.vc
                 run_step(db, stream)
-                out_alen.copy_(db.accept_len, non_blocking=True)
-                out_tok.copy_(db.accepted_tokens, non_blocking=True)
-                if s >= args.warmup:
-                    ev[s - args.warmup][1].record(stream)
+                with torch.cuda.stream(stream):
+                    outs[i][0].copy_(db.accept_len, non_blocking=True)
+                    outs[i][1].copy_(db.accepted_tokens, non_blocking=True)
+                ev_free = torch.cuda.Event()
+                ev_free.record(stream)
+                freed[i] = ev_free
+
+        pipelined(args.warmup)
         torch.cuda.synchronize()
-        e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        copy_stream.wait_event(t0)
+        pipelined(args.steps)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        for k in in_names:
+            setattr(db, k, bufs[0][k])
+        db.prefix_len = db.vc
+        e_ms = reduce_max(t0.elapsed_time(t1), dev)
         e2e = {"value": whole_job_rows_per_s(rows_per_step, world, e_ms / args.steps), "unit": "rows/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
+               "pipelined": "inputs double-buffered; upload of step k+1 overlaps step k",
+               "l2": "not flushed: every step streams the 1.1 GB K/V cache, far above L2"}
     check_device_error(db, "the timed steps")
 
     line = {
