@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-argmax", action="store_true", help="skip the target-argmax measurement")
     ap.add_argument("--no-lanes", action="store_true", help="skip the draft-lane attention measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-KV attention measurement")
     return ap.parse_args()
 
 
@@ -432,6 +433,8 @@ def run_ours(args, rank, world, local_rank):
         line["target_argmax"] = time_target_argmax(inp, db, stream, flush, args, hbm)
     if not args.no_lanes:
         line["lane_attention"] = time_lane_attention(stream, flush, args, hbm, tf_sus, db.device)
+    if not args.no_fp8:
+        line["fp8_attention"] = time_fp8_attention(inp, db, stream, flush, args, hbm, tf_sus)
     clocks = clk.summary()
     if clocks is not None:
         line["clocks"] = clocks
@@ -557,6 +560,52 @@ def time_lane_attention(stream, flush, args, hbm, tf_sus, device):
     gbs = nbytes / (us / 1e6) / 1e9
     return {"workload": lw.name, "B": B, "R": R, "W": W, "prefix_len": int(P.max()), "us": us,
             "rows_per_s": B * R / (us / 1e6), "bytes": nbytes, "flops": flops,
+            "roofline": {"bound": "hbm" if t_hbm >= t_mma else "tensor", "achieved": gbs, "peak": hbm,
+                         "unit": "GB/s", "frac": gbs / hbm}, "reps": reps}
+
+
+def time_fp8_attention(inp, db, stream, flush, args, hbm, tf_sus):
+    """tree_verify_attention_fp8 on the bench workload's shape with unscaled
+    E4M3 K/V caches (seeded, N(0,1)-shaped), outside the headline step:
+    CUDA-event time per call, L2 flushed before each. The step's own mask,
+    positions and queries are reused. Roofline as for the bf16 call with one
+    byte per K/V element."""
+    import torch
+    from draft_tree_speculative_gb300 import tree_verify_attention_fp8
+    w = inp.w
+    k8, v8 = synth.fp8_kv_cache(w.index, inp.layout.num_slots, w.Hkv, w.d)
+    kc, vc = torch.from_numpy(k8).to(db.device), torch.from_numpy(v8).to(db.device)
+    del k8, v8
+    BN = w.B * w.N
+    out = torch.empty((BN, w.Hq, w.d), dtype=torch.bfloat16, device=db.device)
+    lse = torch.empty((BN, w.Hq), dtype=torch.float32, device=db.device)
+    err = torch.zeros(1, dtype=torch.int32, device=db.device)
+    reps = max(5, min(args.steps, 50))
+    call = lambda: tree_verify_attention_fp8(db.q, kc, vc, db.page_table, w.page_size, db.prefix_len, db.max_prefix,
+                                             db.mask, db.positions, w.rope_theta, out, lse, db.workspace, err=err,
+                                             stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            call()
+            b.record(stream)
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError(f"device reported error {int(err.item())} in the FP8 attention")
+    us = statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
+    P = inp.vc.astype(np.int64)
+    kv = 2 * w.Hkv * w.d * 1 * (int(P.sum()) + BN)
+    rows = BN * w.Hq
+    nbytes = kv + 2 * rows * w.d * 2 + rows * 4 + BN * (8 + 4) + inp.layout.page_table.size * 4 + w.B * 4
+    flops = 4 * w.N * w.Hq * w.d * int(P.sum())
+    t_hbm, t_mma = nbytes / (hbm * 1e9), flops / (tf_sus * 1e12)
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"workload": w.name, "kv_dtype": "e4m3 (unscaled)", "compute": "f16 MMAs, fp32 accumulation",
+            "us": us, "rows_per_s": BN / (us / 1e6), "bytes": nbytes, "flops": flops,
             "roofline": {"bound": "hbm" if t_hbm >= t_mma else "tensor", "achieved": gbs, "peak": hbm,
                          "unit": "GB/s", "frac": gbs / hbm}, "reps": reps}
 

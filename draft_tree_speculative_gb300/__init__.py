@@ -27,7 +27,8 @@ EXPORTED = (
     "dts_verify_tree_greedy", "dts_compact_window_rows", "dts_compact_rows",
     "dts_tree_verify_attention_static_ws", "dts_target_argmax_workspace", "dts_target_argmax",
     "dts_verify_tree_greedy_logits", "dts_tree_window_attention_workspace", "dts_tree_window_attention",
-    "dts_sample_draws", "dts_verify_tree_sampled",
+    "dts_sample_draws", "dts_verify_tree_sampled", "dts_write_window_kv_fp8", "dts_tree_window_attention_fp8",
+    "dts_tree_verify_attention_fp8",
 )
 
 
@@ -57,6 +58,11 @@ _SIGS = {
     "dts_tree_window_attention_workspace": (_SZ, [_I, _I, _I, _I, _I, _I, _L]),
     "dts_tree_window_attention": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I, _I, _F,
                                        _P, _P, _P, _SZ, _P, _P]),
+    "dts_write_window_kv_fp8": (_I, [_P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _L, _F, _P, _P, _P, _P, _P]),
+    "dts_tree_window_attention_fp8": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I, _I,
+                                           _F, _P, _P, _P, _SZ, _P, _P]),
+    "dts_tree_verify_attention_fp8": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I, _F,
+                                           _P, _P, _P, _SZ, _P, _P]),
     "dts_tree_verify_attention_static_ws": (_I, [_P, _P, _P, _L, _P, _I, _I, _P, _L, _P, _P, _F, _I, _I, _I, _I, _I,
                                                  _F, _P, _P, _P, _P]),
     "dts_verify_tree_greedy": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
@@ -247,6 +253,79 @@ def tree_window_attention(q, k_cache, v_cache, page_table, page_size, prefix_len
         _ptr(prefix_len), int(max_prefix), _ptr(mask), _ptr(positions), float(rope_theta), B, R, int(W), Hq, Hkv, d,
         float(softmax_scale), _ptr(out), _ptr(lse2), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
     _raise(st, "tree_window_attention")
+
+
+def _fp8_cache(torch):
+    """An E4M3 cache is passed as torch.float8_e4m3fn or as its raw bytes (uint8)."""
+    return (torch.float8_e4m3fn, torch.uint8)
+
+
+def write_window_kv_fp8(k_new, v_new, positions, page_table, page_size, prefix_len, k_cache, v_cache,
+                        rope_theta, write_locations=None, err=None, stream=None, N=None):
+    """write_window_kv into E4M3 caches (include/dts.h, dts_write_window_kv_fp8)."""
+    torch = _torch()
+    BN, Hkv, d = k_new.shape
+    B = prefix_len.shape[0]
+    N = BN // B if N is None else N
+    _check(k_new, torch.bfloat16, (BN, Hkv, d), "k_new")
+    _check(v_new, torch.bfloat16, (BN, Hkv, d), "v_new")
+    _check(positions, _i32(), None, "positions")
+    _check(page_table, _i32(), None, "page_table")
+    _check(k_cache, _fp8_cache(torch), None, "k_cache")
+    _check(v_cache, _fp8_cache(torch), tuple(k_cache.shape), "v_cache")
+    _check(write_locations, torch.int64, (BN,), "write_locations")
+    st = lib().dts_write_window_kv_fp8(_ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(page_table),
+                                       page_table.shape[1], page_size, _ptr(prefix_len), B, N, Hkv, d,
+                                       k_cache.shape[0], float(rope_theta), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(write_locations), _ptr(err), _stream(stream))
+    _raise(st, "write_window_kv_fp8")
+
+
+def tree_window_attention_fp8(q, k_cache, v_cache, page_table, page_size, prefix_len, max_prefix, mask, positions,
+                              rope_theta, out, lse2, workspace, W, softmax_scale=0.0, err=None, stream=None):
+    """tree_window_attention over E4M3 caches (include/dts.h, dts_tree_window_attention_fp8)."""
+    torch = _torch()
+    BR, Hq, d = q.shape
+    B = prefix_len.shape[0]
+    if BR % B:
+        raise ValueError("q rows must be a multiple of B")
+    R = BR // B
+    Hkv = k_cache.shape[1]
+    _check(q, torch.bfloat16, (BR, Hq, d), "q")
+    _check(k_cache, _fp8_cache(torch), None, "k_cache")
+    _check(v_cache, _fp8_cache(torch), tuple(k_cache.shape), "v_cache")
+    _check(mask, _u64(), (B, R), "mask")
+    _check(positions, _i32(), (B, R), "positions")
+    _check(out, torch.bfloat16, (BR, Hq, d), "out")
+    _check(lse2, torch.float32, (BR, Hq), "lse2")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().dts_tree_window_attention_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(page_table), page_table.shape[1], page_size,
+        _ptr(prefix_len), int(max_prefix), _ptr(mask), _ptr(positions), float(rope_theta), B, R, int(W), Hq, Hkv, d,
+        float(softmax_scale), _ptr(out), _ptr(lse2), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
+    _raise(st, "tree_window_attention_fp8")
+
+
+def tree_verify_attention_fp8(q, k_cache, v_cache, page_table, page_size, prefix_len, max_prefix, mask, positions,
+                              rope_theta, out, lse2, workspace, softmax_scale=0.0, err=None, stream=None, N=None):
+    """tree_verify_attention over E4M3 caches (include/dts.h, dts_tree_verify_attention_fp8)."""
+    torch = _torch()
+    BN, Hq, d = q.shape
+    B = prefix_len.shape[0]
+    N = BN // B if N is None else N
+    Hkv = k_cache.shape[1]
+    _check(q, torch.bfloat16, (BN, Hq, d), "q")
+    _check(k_cache, _fp8_cache(torch), None, "k_cache")
+    _check(v_cache, _fp8_cache(torch), tuple(k_cache.shape), "v_cache")
+    _check(mask, _u64(), None, "mask")
+    _check(out, torch.bfloat16, (BN, Hq, d), "out")
+    _check(lse2, torch.float32, (BN, Hq), "lse2")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().dts_tree_verify_attention_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(page_table), page_table.shape[1], page_size,
+        _ptr(prefix_len), int(max_prefix), _ptr(mask), _ptr(positions), float(rope_theta), B, N, Hq, Hkv, d,
+        float(softmax_scale), _ptr(out), _ptr(lse2), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
+    _raise(st, "tree_verify_attention_fp8")
 
 
 def tree_verify_attention_static_ws(q, k_cache, v_cache, page_table, page_size, prefix_len, max_prefix, mask,

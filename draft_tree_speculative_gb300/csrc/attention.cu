@@ -96,6 +96,7 @@ struct PrepArgs {
   int32_t *err;
   int64_t max_prefix, capacity;  // capacity: page-table rows x page size
   int rows, R, W, Hq, heads_per_thread;   // rows = B*R query rows; W window keys per request
+  int to_e4m3;  // FP8 cache: store the (rotated, bf16-rounded) queries as E4M3 bytes
   dts::RopeFreqs freqs;
 };
 
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
   const int P = a.prefix_len[b];
   const int pos = a.positions != nullptr ? a.positions[node] : 0;
   uint4 x1[kMaxHeads], x2[kMaxHeads];
-  if (a.positions != nullptr) {
+  if (a.positions != nullptr || a.to_e4m3) {
 #pragma unroll
     for (int hh = 0; hh < kMaxHeads; ++hh) {
       if (hh >= a.heads_per_thread) break;
@@ -139,10 +140,12 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
     }
     return;
   }
-  if (a.positions == nullptr) return;
+  if (a.positions == nullptr && !a.to_e4m3) return;
   float sn[8], cs[8];
+  if (a.positions != nullptr) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) dts::rope_sincos(pos, a.freqs.w[8 * c + e], &sn[e], &cs[e]);
+    for (int e = 0; e < 8; ++e) dts::rope_sincos(pos, a.freqs.w[8 * c + e], &sn[e], &cs[e]);
+  }
 #pragma unroll
   for (int hh = 0; hh < kMaxHeads; ++hh) {
     if (hh >= a.heads_per_thread) break;
@@ -150,13 +153,30 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
     uint32_t *w2 = reinterpret_cast<uint32_t *>(&x2[hh]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float u0 = dts::bf16_lo(w1[e]), u1 = dts::bf16_hi(w1[e]);
-      const float v0 = dts::bf16_lo(w2[e]), v1 = dts::bf16_hi(w2[e]);
-      const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
-      w1[e] = dts::pack_bf16x2(u0 * c0 - v0 * s0, u1 * c1 - v1 * s1);
-      w2[e] = dts::pack_bf16x2(v0 * c0 + u0 * s0, v1 * c1 + u1 * s1);
+      if (a.positions != nullptr) {
+        const float u0 = dts::bf16_lo(w1[e]), u1 = dts::bf16_hi(w1[e]);
+        const float v0 = dts::bf16_lo(w2[e]), v1 = dts::bf16_hi(w2[e]);
+        const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
+        w1[e] = dts::pack_bf16x2(u0 * c0 - v0 * s0, u1 * c1 - v1 * s1);
+        w2[e] = dts::pack_bf16x2(v0 * c0 + u0 * s0, v1 * c1 + u1 * s1);
+      }
     }
     const int64_t off = (node * a.Hq + hg * a.heads_per_thread + hh) * D + 8 * c;
+    if (a.to_e4m3) {
+      // the bf16 values cast to E4M3 (nearest even, saturating): 8 bytes a half
+      uint8_t *q8 = reinterpret_cast<uint8_t *>(a.q_rot);
+      uint32_t b1[2], b2[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        b1[e] = dts::f32x2_to_e4m3x2(dts::bf16_lo(w1[2 * e]), dts::bf16_hi(w1[2 * e])) |
+                (dts::f32x2_to_e4m3x2(dts::bf16_lo(w1[2 * e + 1]), dts::bf16_hi(w1[2 * e + 1])) << 16);
+        b2[e] = dts::f32x2_to_e4m3x2(dts::bf16_lo(w2[2 * e]), dts::bf16_hi(w2[2 * e])) |
+                (dts::f32x2_to_e4m3x2(dts::bf16_lo(w2[2 * e + 1]), dts::bf16_hi(w2[2 * e + 1])) << 16);
+      }
+      *reinterpret_cast<uint2 *>(q8 + off) = make_uint2(b1[0], b1[1]);
+      *reinterpret_cast<uint2 *>(q8 + off + D / 2) = make_uint2(b2[0], b2[1]);
+      continue;
+    }
     *reinterpret_cast<uint4 *>(a.q_rot + off) = x1[hh];
     *reinterpret_cast<uint4 *>(a.q_rot + off + D / 2) = x2[hh];
   }
@@ -187,9 +207,9 @@ struct PrefixShape {
   static constexpr uint32_t kBlockBytes = 128 * 128;   // one 64-column block of a 128-row tile
   static constexpr int kSlots = D == 128 ? 5 : 8;      // K/V ring
   static constexpr uint32_t kBarBytes = 512;
-  // kfull, vfull, empty, vready rings, 12 single barriers, the poison mask,
+  // kfull, vfull, empty, vready rings, 12 single barriers, two poison masks,
   // the tile total (two words) and the TMEM address / abort flag words
-  static_assert((4 * kSlots + 12) * 8 + 8 + 16 + 8 <= kBarBytes, "barrier area too small");
+  static_assert((4 * kSlots + 12) * 8 + 16 + 16 + 8 <= kBarBytes, "barrier area too small");
   static constexpr uint32_t kSmem = 1024 /*align*/ + 2 * kTileBytes + kSlots * kTileBytes + kBarBytes;
 };
 
@@ -316,7 +336,84 @@ __device__ __forceinline__ uint64_t clean_window_v(uint8_t *vt, int o, int W, in
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
-template <int D>
+// FP8 cache: widens, in place, rows [r0, r0 + 64) of the E4M3 V tile that
+// TMA left in the slot's second half (128 rows of 128 bytes, 128-byte
+// swizzle) into the layout of a bf16 tile (two 64-column blocks, same
+// swizzle) holding f16 values, exact for every E4M3 value. Lane l takes rows
+// r0 + l and r0 + l + 32 and reads a whole row before writing it; the row's
+// second f16 block is the only place where its output overlaps the input,
+// and that is the row's own bytes. Rows past the unit's keys become zero, and
+// a window key (tile reaching the window, window index o of its first row)
+// with a NaN byte gets a zero row and a bit in the returned mask, as
+// clean_window_v does for a bf16 tile.
+__device__ __forceinline__ uint64_t widen_fp8_v_rows(uint8_t *tile, int r0, int nvalid, int o, bool window,
+                                                     int lane) {
+  constexpr uint32_t kBlockBytes = 128 * 128;
+  uint64_t bad_keys = 0;
+#pragma unroll 1
+  for (int x = r0 + lane; x < r0 + 64; x += 32) {
+    const uint32_t sw = static_cast<uint32_t>(x & 7);
+    uint4 *row0 = reinterpret_cast<uint4 *>(tile + x * 128);                // f16 columns 0..63
+    uint4 *row1 = reinterpret_cast<uint4 *>(tile + kBlockBytes + x * 128);  // 64..127; the E4M3 row on entry
+    if (x >= nvalid) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        row0[c] = make_uint4(0, 0, 0, 0);
+        row1[c] = make_uint4(0, 0, 0, 0);
+      }
+      continue;
+    }
+    uint4 in[8];  // 16-byte chunk c holds elements 16c .. 16c + 15
+#pragma unroll
+    for (int c = 0; c < 8; ++c) in[c] = row1[c ^ sw];
+    bool zero = false;
+    if (window && x >= -o) {
+      uint32_t nan_bytes = 0;  // a byte whose low seven bits are all set (S.1111.111)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t w[4] = {in[c].x, in[c].y, in[c].z, in[c].w};
+#pragma unroll
+        for (int f = 0; f < 4; ++f) {
+          const uint32_t t = (w[f] & 0x7F7F7F7Fu) ^ 0x7F7F7F7Fu;
+          nan_bytes |= (t - 0x01010101u) & ~t & 0x80808080u;
+        }
+      }
+      if (nan_bytes != 0u) {
+        zero = true;
+        bad_keys |= 1ull << (o + x);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w[4] = {in[c].x, in[c].y, in[c].z, in[c].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        h[2 * f] = zero ? 0u : dts::e4m3x2_to_f16x2(w[f] & 0xFFFFu);
+        h[2 * f + 1] = zero ? 0u : dts::e4m3x2_to_f16x2(w[f] >> 16);
+      }
+      // elements 16c .. 16c + 15 are f16 chunks 2c and 2c + 1 of the row:
+      // block c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1 inside it
+      uint4 *dst = c < 4 ? row0 : row1;
+      const uint32_t c0 = 2u * static_cast<uint32_t>(c & 3);
+      dst[c0 ^ sw] = make_uint4(h[0], h[1], h[2], h[3]);
+      dst[(c0 + 1u) ^ sw] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+  fence_proxy_async();  // the widened rows are read by the tensor core
+  __syncwarp();
+  const uint32_t lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bad_keys));
+  const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bad_keys >> 32));
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// F8: the K and V caches hold unscaled E4M3 bytes ([TS] "One tree attention",
+// FP8 paragraph: no structural change; the prefix decode takes the query cast
+// to FP8; the window's FP8 K/V are widened after loading). S = Q K^T runs as
+// an FP8 MMA (kind::f8f6f4) on the E4M3 query (rotated, rounded to bf16, then
+// cast) and the K tile as loaded. Warps 2 and 3 widen each V tile to f16 in
+// shared memory (64 rows each), and O += P V runs in f16 with P in f16.
+template <int D, bool F8>
 __global__ void __launch_bounds__(384, 1)
     tree_prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ PrefixArgs a) {
@@ -347,8 +444,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t *drain = q_empty + 1;
   uint64_t *win_bar = drain + 1;                             // the segment's poisoned-key mask is written
   uint64_t *vready = win_bar + 1;                            // [kSlots] a V tile landed and is clean
-  uint64_t *poison = vready + kSlots;                        // window keys whose V rows were not finite
-  int64_t *range = reinterpret_cast<int64_t *>(poison + 1);  // [0] = total tiles
+  uint64_t *poison = vready + kSlots;                        // [2] window keys whose V rows were not finite
+  int64_t *range = reinterpret_cast<int64_t *>(poison + 2);  // [0] = total tiles
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(range + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -367,8 +464,10 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(drain, 1);
-    mbar_init(win_bar, 1);
-    for (int s2 = 0; s2 < kSlots; ++s2) mbar_init(&vready[s2], 1);
+    // F8: both V warps (2 and 3) arrive on vready and win_bar
+    mbar_init(win_bar, F8 ? 2 : 1);
+    for (int s2 = 0; s2 < kSlots; ++s2) mbar_init(&vready[s2], F8 ? 2 : 1);
+    poison[1] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -424,6 +523,10 @@ __global__ void __launch_bounds__(384, 1)
       const int ps = 1 << a.page_shift;
       const int rows_per_box = ps < 128 ? ps : 128;
       const int boxes = 128 / rows_per_box;
+      // a Q, K or V row is D / 64 boxes of 64 bf16 columns, or one box of
+      // D = 128 E4M3 bytes; an E4M3 V tile lands in the slot's second half, to
+      // be widened there
+      constexpr int kRowBoxes = F8 ? 1 : D / 64;
       int use = 0, segc = 0;
       bool ok = true;
       while (ok && walker.next(a, sg)) {
@@ -453,10 +556,10 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         if (lane == 0) {
-          mbar_expect_tx(q_full, static_cast<uint32_t>(sg.nt * (D / 64) * a.rt * 128));
+          mbar_expect_tx(q_full, static_cast<uint32_t>(sg.nt * kRowBoxes * a.rt * 128));
           for (int t = 0; t < sg.nt; ++t) {
             const int node0 = (sg.pair * 2 + t) * a.npt;
-            for (int h = 0; h < D / 64; ++h)
+            for (int h = 0; h < kRowBoxes; ++h)
               tma_load_4d(sQ_addr + t * kTileBytes + h * S::kBlockBytes, &tm_q, h * 64, 0, sg.hkv,
                           sg.b * a.R + node0, q_full);
           }
@@ -476,13 +579,13 @@ __global__ void __launch_bounds__(384, 1)
             }
             uint64_t *done = kv == 0 ? &kfull[slot] : &vfull[slot];
             if (lane == 0)  // the barrier expects exactly the bytes of the boxes issued below
-              mbar_expect_tx(done, static_cast<uint32_t>(nbox * rows_per_box * 128 * (D / 64)));
+              mbar_expect_tx(done, static_cast<uint32_t>(nbox * rows_per_box * 128 * kRowBoxes));
             const CUtensorMap *map = kv == 0 ? &tm_k : &tm_v;
-            const uint32_t dst = sKV_addr + slot * kTileBytes;
+            const uint32_t dst = sKV_addr + slot * kTileBytes + (F8 && kv == 1 ? S::kBlockBytes : 0u);
             for (int r = 0; r < boxes; ++r) {
               const int s0 = box_slot(kbase, nvalid, r);
               if (s0 < 0 || lane != 0) continue;
-              for (int h = 0; h < D / 64; ++h)
+              for (int h = 0; h < kRowBoxes; ++h)
                 tma_load_3d(dst + h * S::kBlockBytes + r * rows_per_box * 128, map, h * 64, sg.hkv, s0, done);
             }
             __syncwarp();
@@ -500,8 +603,8 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
-      constexpr uint32_t kIdescO = idesc_bf16(128, D, true);
+      constexpr uint32_t kIdescS = F8 ? idesc_f16(128, 128, false) : idesc_bf16(128, 128, false);  // F8: E4M3
+      constexpr uint32_t kIdescO = F8 ? idesc_f16(128, D, true) : idesc_bf16(128, D, true);
       auto slot_of = [](int use) { return use % kSlots; };
       auto kind_phase_of = [](int use) { return kind_phase<kSlots>(use); };
       // One thread issues every MMA, so the issue loop must stay short: the
@@ -515,10 +618,16 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t qa = q_desc0 + static_cast<uint64_t>(t) * kTileStep;
         const uint64_t kb = k_desc0 + static_cast<uint64_t>(slot) * kTileStep;
         const uint32_t d_tmem = tmem + t * 256;
+        if constexpr (F8) {
+          // one 128-byte E4M3 row per query and key: four K-steps of 32
 #pragma unroll
-        for (int ks = 0; ks < kKSteps; ++ks) {
-          const uint64_t off = ((ks >> 2) * S::kBlockBytes + (ks & 3) * 32) >> 4;
-          mma_ss(d_tmem, qa + off, kb + off, kIdescS, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < 4; ++ks) mma_ss_f8(d_tmem, qa + ks * 2, kb + ks * 2, kIdescS, ks > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < kKSteps; ++ks) {
+            const uint64_t off = ((ks >> 2) * S::kBlockBytes + (ks & 3) * 32) >> 4;
+            mma_ss(d_tmem, qa + off, kb + off, kIdescS, ks > 0 ? 1u : 0u);
+          }
         }
       };
       auto issue_pv = [&](int t, int slot, bool first) {
@@ -607,11 +716,13 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) mma_commit(drain);
       __syncwarp();
       mbar_wait(drain, 0, abort_flag);
-    } else if (warp == 2) {
-      // ---------------------------------------------------------- V-tile warp
+    } else if (warp == 2 || (F8 && warp == 3)) {
+      // ---------------------------------------------------------- V-tile warp(s)
       // Hands every V tile to the MMA warp (vready) once it has landed, after
       // cleaning the ones that reach the window (clean_window_v), and
-      // publishes each segment's poisoned window keys (win_bar).
+      // publishes each segment's poisoned window keys (win_bar). F8: warps 2
+      // and 3 each widen half of every V tile's rows and publish their own mask.
+      const int vw = warp - 2;
       int use = 0, prev_nt = 0;
       int scnt[2] = {0, 0};  // segments each softmax group has taken part in
       bool ok = true;
@@ -624,8 +735,12 @@ __global__ void __launch_bounds__(384, 1)
           ok = mbar_wait(&vfull[vslot], kind_phase<kSlots>(vuse), abort_flag);
           if (!ok) break;
           const int kbase = (sg.lt0 + j) * 128;
-          if (kbase + 128 > sg.P)  // the window's tiles (and the unit's end)
+          if constexpr (F8) {
+            seg_poison |= widen_fp8_v_rows(sKV + vslot * kTileBytes, vw * 64, min(128, sg.P + a.W - kbase),
+                                           kbase - sg.P, kbase + 128 > sg.P, lane);
+          } else if (kbase + 128 > sg.P) {  // the window's tiles (and the unit's end)
             seg_poison |= clean_window_v<D>(sKV + vslot * kTileBytes, kbase - sg.P, a.W, lane);
+          }
           if (lane == 0) mbar_arrive(&vready[vslot]);
           __syncwarp();
         }
@@ -640,7 +755,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int t = 0; t < 2; ++t)
           if (t < sg.nt) ++scnt[t];
         if (lane == 0) {
-          *poison = seg_poison;
+          poison[vw] = seg_poison;
           mbar_arrive(win_bar);
         }
         __syncwarp();
@@ -716,7 +831,7 @@ __global__ void __launch_bounds__(384, 1)
           // -inf, P is 0 and nothing rescales
           const float m_sub = m_use == -INFINITY ? 0.f : m_use;
           const float alpha = m_use == -INFINITY ? 1.f : ex2(m_run - m_use);
-          // P = 2^(s*c - m_use) as bf16 pairs, packed in place over the consumed
+          // P = 2^(s*c - m_use) as bf16 pairs (f16 under F8), packed in place over the consumed
           // S registers: pair (q, k) lands in sv[q >> 1][(q & 1) * 16 + k / 2],
           // an entry already read. The scale-and-shift runs two lanes per FMA.
           const uint64_t cc = f2_pack(c, c);
@@ -738,8 +853,13 @@ __global__ void __launch_bounds__(384, 1)
               b1 = ex2(b1);
               sum0 = fadd2(sum0, f2_pack(a0, a1));
               sum1 = fadd2(sum1, f2_pack(b0, b1));
-              sv[q >> 1][(q & 1) * 16 + (k >> 1)] = dts::pack_bf16x2(a0, a1);
-              sv[q >> 1][(q & 1) * 16 + (k >> 1) + 1] = dts::pack_bf16x2(b0, b1);
+              if constexpr (F8) {
+                sv[q >> 1][(q & 1) * 16 + (k >> 1)] = dts::pack_f16x2(a0, a1);
+                sv[q >> 1][(q & 1) * 16 + (k >> 1) + 1] = dts::pack_f16x2(b0, b1);
+              } else {
+                sv[q >> 1][(q & 1) * 16 + (k >> 1)] = dts::pack_bf16x2(a0, a1);
+                sv[q >> 1][(q & 1) * 16 + (k >> 1) + 1] = dts::pack_bf16x2(b0, b1);
+              }
             }
           float s00, s01, s10, s11;
           f2_unpack(sum0, s00, s01);
@@ -773,7 +893,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_fence_after();
       // a row that sees a window key whose V row was not finite reads NaN
-      const uint64_t seg_poison = *poison;
+      const uint64_t seg_poison = F8 ? (poison[0] | poison[1]) : poison[0];
       const bool poisoned = seg_poison != 0ull && (row_mask() & seg_poison) != 0ull;
       const int node = R / a.g;  // the row's tree node
       const int64_t node_row = static_cast<int64_t>(sg.b) * a.R + node;
@@ -1024,47 +1144,52 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-            const cuuint32_t *box) {
+            const cuuint32_t *box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto enc = get_encode_fn();
   if (enc == nullptr) return false;
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, estr,
+  CUresult r = enc(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// 3-D view (d, Hkv, slots) of a paged bf16 cache; box (64, 1, rows_per_box).
-bool make_cache_map(CUtensorMap *map, const void *base, int d, int Hkv, int64_t num_slots, int rows_per_box) {
+// 3-D view (d, Hkv, slots) of a paged cache; box (64, 1, rows_per_box) for
+// bf16, (128, 1, rows_per_box) for E4M3 bytes: 128 bytes a row either way.
+bool make_cache_map(CUtensorMap *map, const void *base, int d, int Hkv, int64_t num_slots, int rows_per_box,
+                    bool f8) {
+  const cuuint64_t esz = f8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_slots)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hkv) * d * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows_per_box)};
-  return encode(map, base, 3, dims, strides, box);
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(Hkv) * d * esz};
+  cuuint32_t box[3] = {f8 ? 128u : 64u, 1, static_cast<cuuint32_t>(rows_per_box)};
+  return encode(map, base, 3, dims, strides, box, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-// 4-D view (d, g, Hkv, B*N) of the queries [B*N][Hq][d]; box (64, g, 1, npt):
-// one box holds the npt * g rows (node, head-in-group) of a row tile, in that order.
-bool make_q_map(CUtensorMap *map, const void *base, int d, int g, int Hkv, int64_t nodes, int npt) {
+// 4-D view (d, g, Hkv, B*N) of the queries [B*N][Hq][d]; box (64, g, 1, npt)
+// of bf16, or (128, g, 1, npt) of E4M3 bytes: one box holds the npt * g rows
+// (node, head-in-group) of a row tile, in that order.
+bool make_q_map(CUtensorMap *map, const void *base, int d, int g, int Hkv, int64_t nodes, int npt, bool f8) {
+  const cuuint64_t esz = f8 ? 1 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(nodes)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(g) * d * 2,
-                           static_cast<cuuint64_t>(g) * Hkv * d * 2};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(npt)};
-  return encode(map, base, 4, dims, strides, box);
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(g) * d * esz,
+                           static_cast<cuuint64_t>(g) * Hkv * d * esz};
+  cuuint32_t box[4] = {f8 ? 128u : 64u, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(npt)};
+  return encode(map, base, 4, dims, strides, box, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-template <int D>
+template <int D, bool F8>
 int launch_prefix(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const PrefixArgs &a, int grid,
                   cudaStream_t s) {
   using S = PrefixShape<D>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(tree_prefix_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(tree_prefix_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(S::kSmem));
   });
   if (attr_err != cudaSuccess) return DTS_ERR_CUDA;
-  tree_prefix_kernel<D><<<grid, S::kThreads, S::kSmem, s>>>(tk, tv, tq, a);
+  tree_prefix_kernel<D, F8><<<grid, S::kThreads, S::kSmem, s>>>(tk, tv, tq, a);
   return dts_host::launch_status();
 }
 
@@ -1082,16 +1207,18 @@ extern "C" size_t dts_tree_verify_attention_workspace(int B, int N, int Hq, int 
   return dts_tree_window_attention_workspace(B, N, N, Hq, Hkv, d, max_prefix);
 }
 
-extern "C" int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                                         int64_t num_slots, const int32_t *page_table, int max_pages,
-                                         int page_size, const int32_t *prefix_len, int64_t max_prefix,
-                                         const uint64_t *mask, const int32_t *positions, float rope_theta,
-                                         int B, int R, int W, int Hq, int Hkv, int d, float softmax_scale,
-                                         uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
-                                         int32_t *err_dev, dts_stream_t stream) {
+namespace {
+
+// Both cache types: bf16 (f8 = false) or unscaled E4M3 bytes (f8 = true).
+int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void *v_cache, int64_t num_slots,
+                     const int32_t *page_table, int max_pages, int page_size, const int32_t *prefix_len,
+                     int64_t max_prefix, const uint64_t *mask, const int32_t *positions, float rope_theta, int B, int R,
+                     int W, int Hq, int Hkv, int d, float softmax_scale, uint16_t *out, float *lse2, void *workspace,
+                     size_t ws_bytes, int32_t *err_dev, dts_stream_t stream) {
   if (B < 0 || R < 1 || W < 1 || Hkv < 1 || Hq < 1 || max_pages < 1 || num_slots < 1 || max_prefix < 0)
     return DTS_ERR_INVALID;
   if (R > dts::kMaxNodes || W > dts::kMaxNodes || (d != 64 && d != 128)) return DTS_ERR_UNSUPPORTED;
+  if (f8 && d != 128) return DTS_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return DTS_ERR_INVALID;
   if (Hq / Hkv > 128) return DTS_ERR_UNSUPPORTED;
   if (page_size < 8 || page_size > 4096 || (page_size & (page_size - 1)) != 0) return DTS_ERR_UNSUPPORTED;
@@ -1133,6 +1260,7 @@ extern "C" int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_ca
     ra.W = W;
     ra.Hq = Hq;
     ra.heads_per_thread = (Hq % 4 == 0) ? 4 : (Hq % 2 == 0) ? 2 : 1;
+    ra.to_e4m3 = f8 ? 1 : 0;
     if (positions != nullptr) dts_host::make_rope_freqs(rope_theta, d, &ra.freqs);
     const int64_t items = static_cast<int64_t>(B) * R * (Hq / ra.heads_per_thread) * (d / 16);
     const int blocks = static_cast<int>((items + 255) / 256);
@@ -1140,15 +1268,16 @@ extern "C" int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_ca
     else attn_prep_kernel<64><<<blocks, 256, 0, s>>>(ra);
     if (dts_host::launch_status() != DTS_OK) return DTS_ERR_CUDA;
   }
-  const uint16_t *q_eff = positions != nullptr ? q_rot : q;
+  const uint16_t *q_eff = (positions != nullptr || f8) ? q_rot : q;
 
   // 1. tree attention, one CTA per SM
   const int sms = dts_host::sm_count();
   const int grid = sms > 0 ? (sms < kMaxGrid ? sms : kMaxGrid) : 1;
   CUtensorMap tk, tv, tq;
   const int rpb = page_size < 128 ? page_size : 128;
-  if (!make_cache_map(&tk, k_cache, d, Hkv, num_slots, rpb) || !make_cache_map(&tv, v_cache, d, Hkv, num_slots, rpb) ||
-      !make_q_map(&tq, q_eff, d, g, Hkv, static_cast<int64_t>(B) * R, plan.npt))
+  if (!make_cache_map(&tk, k_cache, d, Hkv, num_slots, rpb, f8) ||
+      !make_cache_map(&tv, v_cache, d, Hkv, num_slots, rpb, f8) ||
+      !make_q_map(&tq, q_eff, d, g, Hkv, static_cast<int64_t>(B) * R, plan.npt, f8))
     return DTS_ERR_CUDA;
   PrefixArgs pa;
   pa.page_table = page_table;
@@ -1176,7 +1305,9 @@ extern "C" int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_ca
   pa.max_pages = max_pages;
   pa.page_shift = page_shift;
   pa.scale_log2 = scale * kLog2e;
-  const int st = d == 128 ? launch_prefix<128>(tk, tv, tq, pa, grid, s) : launch_prefix<64>(tk, tv, tq, pa, grid, s);
+  const int st = f8          ? launch_prefix<128, true>(tk, tv, tq, pa, grid, s)
+                 : d == 128 ? launch_prefix<128, false>(tk, tv, tq, pa, grid, s)
+                            : launch_prefix<64, false>(tk, tv, tq, pa, grid, s);
   if (st != DTS_OK) return st;
 
   // 2. merge pass: units whose key tiles went to more than one CTA
@@ -1210,6 +1341,44 @@ extern "C" int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_ca
   if (d == 128) tree_merge_kernel<128><<<blocks, 256, 0, s>>>(ma);
   else tree_merge_kernel<64><<<blocks, 256, 0, s>>>(ma);
   return dts_host::launch_status();
+}
+
+}  // namespace
+
+extern "C" int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                         int64_t num_slots, const int32_t *page_table, int max_pages,
+                                         int page_size, const int32_t *prefix_len, int64_t max_prefix,
+                                         const uint64_t *mask, const int32_t *positions, float rope_theta,
+                                         int B, int R, int W, int Hq, int Hkv, int d, float softmax_scale,
+                                         uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
+                                         int32_t *err_dev, dts_stream_t stream) {
+  return window_attention(false, q, k_cache, v_cache, num_slots, page_table, max_pages, page_size, prefix_len,
+                          max_prefix, mask, positions, rope_theta, B, R, W, Hq, Hkv, d, softmax_scale, out, lse2,
+                          workspace, ws_bytes, err_dev, stream);
+}
+
+extern "C" int dts_tree_window_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                             int64_t num_slots, const int32_t *page_table, int max_pages,
+                                             int page_size, const int32_t *prefix_len, int64_t max_prefix,
+                                             const uint64_t *mask, const int32_t *positions, float rope_theta,
+                                             int B, int R, int W, int Hq, int Hkv, int d, float softmax_scale,
+                                             uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
+                                             int32_t *err_dev, dts_stream_t stream) {
+  return window_attention(true, q, k_cache, v_cache, num_slots, page_table, max_pages, page_size, prefix_len,
+                          max_prefix, mask, positions, rope_theta, B, R, W, Hq, Hkv, d, softmax_scale, out, lse2,
+                          workspace, ws_bytes, err_dev, stream);
+}
+
+extern "C" int dts_tree_verify_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                             int64_t num_slots, const int32_t *page_table, int max_pages,
+                                             int page_size, const int32_t *prefix_len, int64_t max_prefix,
+                                             const uint64_t *mask, const int32_t *positions, float rope_theta,
+                                             int B, int N, int Hq, int Hkv, int d, float softmax_scale,
+                                             uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
+                                             int32_t *err_dev, dts_stream_t stream) {
+  return window_attention(true, q, k_cache, v_cache, num_slots, page_table, max_pages, page_size, prefix_len,
+                          max_prefix, mask, positions, rope_theta, B, N, N, Hq, Hkv, d, softmax_scale, out, lse2,
+                          workspace, ws_bytes, err_dev, stream);
 }
 
 extern "C" int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,

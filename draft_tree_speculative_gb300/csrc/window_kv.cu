@@ -4,6 +4,10 @@
 //
 // One warp per node, all its KV heads. Lane l holds the rotate-half pairs
 // (2l, 2l+1 | d/2+2l, d/2+2l+1) for d = 128, or (l | d/2+l) for d = 64.
+//
+// An FP8 cache ([TS] "One tree attention", FP8 paragraph: E4M3, unscaled)
+// stores the same values cast to E4M3: the rotated key as rounded to bf16,
+// and the value, each rounded to nearest even and saturated at +-448.
 #include "common.cuh"
 
 namespace {
@@ -14,8 +18,8 @@ struct WindowKvArgs {
   const int32_t *positions;
   const int32_t *page_table;
   const int32_t *prefix_len;
-  uint16_t *k_cache;
-  uint16_t *v_cache;
+  void *k_cache;  // bf16, or E4M3 bytes (F8)
+  void *v_cache;
   int64_t *write_locations;
   int32_t *err;
   int64_t num_slots;
@@ -26,8 +30,9 @@ struct WindowKvArgs {
 // One warp per node: the RoPE angles depend on the node only, so they are
 // computed once and applied to all its KV heads; every head's K and V loads
 // are issued before the page-table lookup.
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(256) write_window_kv_kernel(const __grid_constant__ WindowKvArgs a) {
+  static_assert(!F8 || D == 128, "the FP8 cache takes d = 128");
   constexpr int kMaxHeads = 16;  // heads held in registers per pass
   const int node = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // b * N + i
   const int lane = threadIdx.x & 31;
@@ -78,22 +83,37 @@ __global__ void __launch_bounds__(256) write_window_kv_kernel(const __grid_const
 #pragma unroll
       for (int u = 0; u < kMaxHeads; ++u) {
         if (u >= nh) break;
-        uint16_t *kout = a.k_cache + (slot * a.Hkv + h0 + u) * D;
-        uint16_t *vout = a.v_cache + (slot * a.Hkv + h0 + u) * D;
+        const int64_t row = (slot * a.Hkv + h0 + u) * D;
         const float a0 = dts::bf16_lo(k1[u]), a1 = dts::bf16_hi(k1[u]);
         const float b0 = dts::bf16_lo(k2[u]), b1 = dts::bf16_hi(k2[u]);
-        reinterpret_cast<uint32_t *>(kout)[lane] = dts::pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
-        reinterpret_cast<uint32_t *>(kout + 64)[lane] = dts::pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
-        reinterpret_cast<uint2 *>(vout)[lane] = v[u];
+        const uint32_t r1 = dts::pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
+        const uint32_t r2 = dts::pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+        if constexpr (F8) {
+          uint8_t *kout = static_cast<uint8_t *>(a.k_cache) + row;
+          uint8_t *vout = static_cast<uint8_t *>(a.v_cache) + row;
+          reinterpret_cast<uint16_t *>(kout)[lane] =
+              static_cast<uint16_t>(dts::f32x2_to_e4m3x2(dts::bf16_lo(r1), dts::bf16_hi(r1)));
+          reinterpret_cast<uint16_t *>(kout + 64)[lane] =
+              static_cast<uint16_t>(dts::f32x2_to_e4m3x2(dts::bf16_lo(r2), dts::bf16_hi(r2)));
+          const uint32_t v01 = dts::f32x2_to_e4m3x2(dts::bf16_lo(v[u].x), dts::bf16_hi(v[u].x));
+          const uint32_t v23 = dts::f32x2_to_e4m3x2(dts::bf16_lo(v[u].y), dts::bf16_hi(v[u].y));
+          reinterpret_cast<uint32_t *>(vout)[lane] = v01 | (v23 << 16);
+        } else {
+          uint16_t *kout = static_cast<uint16_t *>(a.k_cache) + row;
+          uint16_t *vout = static_cast<uint16_t *>(a.v_cache) + row;
+          reinterpret_cast<uint32_t *>(kout)[lane] = r1;
+          reinterpret_cast<uint32_t *>(kout + 64)[lane] = r2;
+          reinterpret_cast<uint2 *>(vout)[lane] = v[u];
+        }
       }
-    } else {
+    } else if constexpr (!F8) {
       float s0, c0;
       dts::rope_sincos(pos, a.freqs.w[lane], &s0, &c0);
 #pragma unroll
       for (int u = 0; u < kMaxHeads; ++u) {
         if (u >= nh) break;
-        uint16_t *kout = a.k_cache + (slot * a.Hkv + h0 + u) * D;
-        uint16_t *vout = a.v_cache + (slot * a.Hkv + h0 + u) * D;
+        uint16_t *kout = static_cast<uint16_t *>(a.k_cache) + (slot * a.Hkv + h0 + u) * D;
+        uint16_t *vout = static_cast<uint16_t *>(a.v_cache) + (slot * a.Hkv + h0 + u) * D;
         const float a0 = __uint_as_float(k1[u] << 16);
         const float b0 = __uint_as_float(k2[u] << 16);
         const uint32_t r = dts::pack_bf16x2(a0 * c0 - b0 * s0, b0 * c0 + a0 * s0);
@@ -105,16 +125,13 @@ __global__ void __launch_bounds__(256) write_window_kv_kernel(const __grid_const
   }
 }
 
-}  // namespace
-
-extern "C" int dts_write_window_kv(const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
-                                   const int32_t *page_table, int max_pages, int page_size,
-                                   const int32_t *prefix_len, int B, int N, int Hkv, int d,
-                                   int64_t num_slots, float rope_theta, uint16_t *k_cache,
-                                   uint16_t *v_cache, int64_t *write_locations, int32_t *err_dev,
-                                   dts_stream_t stream) {
+int write_window_kv(bool f8, const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
+                    const int32_t *page_table, int max_pages, int page_size, const int32_t *prefix_len, int B, int N,
+                    int Hkv, int d, int64_t num_slots, float rope_theta, void *k_cache, void *v_cache,
+                    int64_t *write_locations, int32_t *err_dev, dts_stream_t stream) {
   if (B < 0 || N < 1 || Hkv < 1 || max_pages < 1 || num_slots < 1) return DTS_ERR_INVALID;
   if (N > dts::kMaxNodes || (d != 64 && d != 128)) return DTS_ERR_UNSUPPORTED;
+  if (f8 && d != 128) return DTS_ERR_UNSUPPORTED;
   if (page_size < 8 || page_size > 4096 || (page_size & (page_size - 1)) != 0) return DTS_ERR_UNSUPPORTED;
   if (!(rope_theta > 0.f)) return DTS_ERR_INVALID;
   if (B == 0) return DTS_OK;
@@ -122,7 +139,7 @@ extern "C" int dts_write_window_kv(const uint16_t *k_new, const uint16_t *v_new,
     return DTS_ERR_INVALID;
   const uintptr_t al = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
                        reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
-  if (al & 7) return DTS_ERR_INVALID;
+  if (al & 7) return DTS_ERR_INVALID;  // (an E4M3 row of 128 bytes keeps every store aligned too)
   WindowKvArgs a;
   a.k_new = k_new;
   a.v_new = v_new;
@@ -143,7 +160,30 @@ extern "C" int dts_write_window_kv(const uint16_t *k_new, const uint16_t *v_new,
   const int64_t warps = static_cast<int64_t>(B) * N;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (d == 128) write_window_kv_kernel<128><<<blocks, 256, 0, s>>>(a);
-  else write_window_kv_kernel<64><<<blocks, 256, 0, s>>>(a);
+  if (f8) write_window_kv_kernel<128, true><<<blocks, 256, 0, s>>>(a);
+  else if (d == 128) write_window_kv_kernel<128, false><<<blocks, 256, 0, s>>>(a);
+  else write_window_kv_kernel<64, false><<<blocks, 256, 0, s>>>(a);
   return dts_host::launch_status();
+}
+
+}  // namespace
+
+extern "C" int dts_write_window_kv(const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
+                                   const int32_t *page_table, int max_pages, int page_size,
+                                   const int32_t *prefix_len, int B, int N, int Hkv, int d,
+                                   int64_t num_slots, float rope_theta, uint16_t *k_cache,
+                                   uint16_t *v_cache, int64_t *write_locations, int32_t *err_dev,
+                                   dts_stream_t stream) {
+  return write_window_kv(false, k_new, v_new, positions, page_table, max_pages, page_size, prefix_len, B, N, Hkv, d,
+                         num_slots, rope_theta, k_cache, v_cache, write_locations, err_dev, stream);
+}
+
+extern "C" int dts_write_window_kv_fp8(const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
+                                       const int32_t *page_table, int max_pages, int page_size,
+                                       const int32_t *prefix_len, int B, int N, int Hkv, int d,
+                                       int64_t num_slots, float rope_theta, uint8_t *k_cache,
+                                       uint8_t *v_cache, int64_t *write_locations, int32_t *err_dev,
+                                       dts_stream_t stream) {
+  return write_window_kv(true, k_new, v_new, positions, page_table, max_pages, page_size, prefix_len, B, N, Hkv, d,
+                         num_slots, rope_theta, k_cache, v_cache, write_locations, err_dev, stream);
 }

@@ -126,6 +126,31 @@ def normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
     return f32_to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
 
 
+def normal_e4m3(rng: np.random.Generator, shape) -> np.ndarray:
+    """N(0,1)-shaped E4M3 bytes (storage only, no rounding): the sign, the
+    exponent (rebiased from 127 to 7) and the three leading mantissa bits of
+    an fp32 draw. Draws below 2^-6 in magnitude store zero; none of an N(0,1)
+    draw reaches the top binade [256, 512), so no NaN code appears."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint8)
+    step = 1 << 24
+    for o in range(0, n, step):
+        u = rng.standard_normal(size=min(step, n - o), dtype=np.float32).view(np.uint32)
+        e = ((u >> np.uint32(23)) & np.uint32(0xFF)).astype(np.int32) - 120
+        m = ((u >> np.uint32(20)) & np.uint32(7)).astype(np.int32)
+        code = np.where(e < 1, 0, (np.minimum(e, 15) << 3) | m)
+        code = np.minimum(code, 0x7E)
+        out[o:o + step] = (code | ((u >> np.uint32(31)).astype(np.int32) << 7)).astype(np.uint8)
+    return out.reshape(shape)
+
+
+def fp8_kv_cache(index: int, num_slots: int, Hkv: int, d: int):
+    """E4M3 K and V caches [num_slots][Hkv][d] from a workload's k_cache and
+    v_cache streams (every key taken as already rotated at its position)."""
+    s = streams(index)
+    return normal_e4m3(s["k_cache"], (num_slots, Hkv, d)), normal_e4m3(s["v_cache"], (num_slots, Hkv, d))
+
+
 # ----------------------------------------------------------------------------
 # Draft trees (drafter side; produces the verify step's parents/depth inputs)
 # ----------------------------------------------------------------------------
@@ -439,7 +464,7 @@ class LaneInputs:
     positions: np.ndarray   # int32 [B][K]: the lane tokens' positions
     layout: PagedLayout
     q: np.ndarray           # bf16 bits [B*K][Hq][d] (not rotated)
-    k_cache: np.ndarray     # bf16 bits [num_slots][Hkv][d] (all keys already rotated)
+    k_cache: np.ndarray     # bf16 bits, or E4M3 bytes, [num_slots][Hkv][d] (all keys already rotated)
     v_cache: np.ndarray
 
     @property
@@ -447,11 +472,12 @@ class LaneInputs:
         return self.layout.prefix_len
 
 
-def make_lane_inputs(lw: LaneWorkload) -> LaneInputs:
+def make_lane_inputs(lw: LaneWorkload, kv_fp8: bool = False) -> LaneInputs:
     """Seeded lane inputs. The drafter's beam keeps K lanes per step; lane r of
     step s >= 2 descends from a lane of step s - 1 drawn uniformly (several
     lanes may share a parent), and a lane's mask holds its own key's bit and
-    its ancestors' (one per earlier step)."""
+    its ancestors' (one per earlier step). kv_fp8: the caches are E4M3 bytes
+    (normal_e4m3) instead of bf16 bits."""
     s = streams(lw.index)
     B, K, W = lw.B, lw.K, lw.W
     step = lw.step or lw.S - 1
@@ -474,8 +500,9 @@ def make_lane_inputs(lw: LaneWorkload) -> LaneInputs:
     lay = make_layout(w, plen, s["pages"])
     positions = (plen[:, None] + step - 1 + np.zeros((1, K), np.int32)).astype(np.int32)
     q = normal_bf16(s["q"], (B * K, lw.Hq, lw.d))
-    k_cache = normal_bf16(s["k_cache"], (lay.num_slots, lw.Hkv, lw.d))
-    v_cache = normal_bf16(s["v_cache"], (lay.num_slots, lw.Hkv, lw.d))
+    draw = normal_e4m3 if kv_fp8 else normal_bf16
+    k_cache = draw(s["k_cache"], (lay.num_slots, lw.Hkv, lw.d))
+    v_cache = draw(s["v_cache"], (lay.num_slots, lw.Hkv, lw.d))
     return LaneInputs(lw, masks, positions, lay, q, k_cache, v_cache)
 
 

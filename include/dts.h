@@ -12,6 +12,8 @@
  *                               its own ancestors; out + base-2 LSE
  *   dts_tree_window_attention   the same over R rows and a W-key masked window
  *                               (draft lanes: R = K rows, W = (S - 1) * K keys)
+ *   dts_*_fp8                   the window write and both attentions over an
+ *                               unscaled FP8-E4M3 KV cache
  *   dts_verify_tree_greedy      greedy walk -> accept_len, packed path, tokens
  *   dts_target_argmax           the target's argmax per verify row (and
  *   dts_verify_tree_greedy_logits  that argmax fed straight into the walk)
@@ -236,6 +238,59 @@ int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_cache,
                               int B, int R, int W, int Hq, int Hkv, int d, float softmax_scale,
                               uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
                               int32_t *err_dev, dts_stream_t stream);
+
+/*
+ * FP8-E4M3 KV cache.
+ *
+ * Defined by [TS] "One tree attention", FP8 paragraph: an FP8 KV cache is
+ * E4M3 and unscaled (a byte is the value itself), it changes none of the
+ * structure, and the window's FP8 K/V are widened to the model dtype after
+ * loading, with the unquantized query. Format: 1 sign bit, 4 exponent bits
+ * (bias 7), 3 mantissa bits, S.1111.111 = NaN, no infinity, largest 448.
+ *
+ * dts_write_window_kv_fp8 - dts_write_window_kv into E4M3 caches
+ * [num_slots][Hkv][d] (bytes). Stored values: the rotated key as rounded to
+ * bf16, then cast to E4M3, and the value cast to E4M3; the cast rounds to
+ * nearest even and saturates at +-448 (NaN stays NaN). d = 128 only
+ * (DTS_ERR_UNSUPPORTED otherwise); every other argument, rule and error is
+ * dts_write_window_kv's.
+ *
+ * dts_tree_window_attention_fp8 / dts_tree_verify_attention_fp8 -
+ * dts_tree_window_attention / dts_tree_verify_attention over E4M3 caches
+ * [num_slots][Hkv][d] (bytes, 16-byte aligned), with the same workspace
+ * sizes (dts_tree_window_attention_workspace /
+ * dts_tree_verify_attention_workspace). The query (rotated and rounded to
+ * bf16 as for the bf16 cache, or as given when positions is NULL) is cast to
+ * E4M3 as the prefix decode over an FP8 cache does, and every key, prefix or
+ * window, is scored against that query: S = Q K^T is one E4M3 tensor-core
+ * product with fp32 accumulation. V is widened to f16 (exact), the softmax
+ * weights enter P.V as f16, accumulation is fp32. d = 128 only
+ * (DTS_ERR_UNSUPPORTED otherwise); every other argument, output rule and error
+ * is that of the bf16 call, a NaN byte in a window key's V row standing for
+ * the non-finite V row there.
+ */
+int dts_write_window_kv_fp8(const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
+                            const int32_t *page_table, int max_pages, int page_size,
+                            const int32_t *prefix_len, int B, int N, int Hkv, int d,
+                            int64_t num_slots, float rope_theta, uint8_t *k_cache,
+                            uint8_t *v_cache, int64_t *write_locations, int32_t *err_dev,
+                            dts_stream_t stream);
+int dts_tree_window_attention_fp8(const uint16_t *q, const uint8_t *k_cache,
+                                  const uint8_t *v_cache, int64_t num_slots,
+                                  const int32_t *page_table, int max_pages, int page_size,
+                                  const int32_t *prefix_len, int64_t max_prefix,
+                                  const uint64_t *mask, const int32_t *positions, float rope_theta,
+                                  int B, int R, int W, int Hq, int Hkv, int d, float softmax_scale,
+                                  uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
+                                  int32_t *err_dev, dts_stream_t stream);
+int dts_tree_verify_attention_fp8(const uint16_t *q, const uint8_t *k_cache,
+                                  const uint8_t *v_cache, int64_t num_slots,
+                                  const int32_t *page_table, int max_pages, int page_size,
+                                  const int32_t *prefix_len, int64_t max_prefix,
+                                  const uint64_t *mask, const int32_t *positions, float rope_theta,
+                                  int B, int N, int Hq, int Hkv, int d, float softmax_scale,
+                                  uint16_t *out, float *lse2, void *workspace, size_t ws_bytes,
+                                  int32_t *err_dev, dts_stream_t stream);
 
 /*
  * dts_tree_verify_attention_static_ws - dts_tree_verify_attention without a

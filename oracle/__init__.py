@@ -27,4 +27,4 @@ log-sum-exp combine rule), ``argmax`` (the target's argmax per verify row and
 the walk fed by it), ``sampling`` (Gumbel-max draws keyed by position and the
 walk over them).
 """
-from . import tree, rope, attention, walk, compact, merge, argmax, sampling  # noqa: F401
+from . import tree, rope, attention, walk, compact, merge, argmax, sampling, fp8  # noqa: F401

@@ -145,7 +145,8 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, page_table, prefix_len, 
 
 def window_attention(q, k_cache, v_cache, page_table, prefix_len, mask, positions, W: int, Hkv: int,
                      theta: float, page_size: int = 64, scale: Optional[float] = None,
-                     q_rotated: bool = False, rope_out: Optional[str] = "bf16"):
+                     q_rotated: bool = False, rope_out: Optional[str] = "bf16", kv_fp8: bool = False,
+                     q_fp8: bool = False):
     """Attention of R query rows per request over the committed prefix plus
     a masked window of W keys, all read from the paged cache.
 
@@ -169,8 +170,18 @@ def window_attention(q, k_cache, v_cache, page_table, prefix_len, mask, position
     [slots][Hkv][d]; page_table [B][max_pages]; prefix_len [B]; mask [B][R]
     (uint64 or Python ints); positions [B][R]. Returns (out [B*R][Hq][d],
     lse2 [B*R][Hq]), fp64.
+
+    ``kv_fp8``: the caches hold E4M3 bytes, read as the values they encode
+    (oracle.fp8.decode_e4m3; [TS] "One tree attention", FP8 paragraph: the
+    cache is unscaled and its K/V are widened after loading). ``q_fp8``: the
+    query (rotated and rounded as above) is cast to E4M3 before the scores
+    (oracle.fp8.encode_e4m3; the same paragraph: the decode over an FP8 cache
+    takes the query cast to FP8).
     """
     rnd = round_bf16 if rope_out == "bf16" else (lambda a: a)
+    if kv_fp8 or q_fp8:
+        from .fp8 import decode_e4m3, encode_e4m3
+    load = decode_e4m3 if kv_fp8 else widen
     q = np.asarray(q)
     B = len(prefix_len)
     R = q.shape[0] // B
@@ -185,16 +196,18 @@ def window_attention(q, k_cache, v_cache, page_table, prefix_len, mask, position
         P = int(prefix_len[b])
         pt = np.asarray(page_table[b], dtype=np.int64)
         slots_all = prefix_slots(pt, P + W, page_size)
-        Kp = widen(kc[slots_all[:P]]).transpose(1, 0, 2)               # [Hkv][P][d]
-        Vp = widen(vc[slots_all[:P]]).transpose(1, 0, 2)
+        Kp = load(kc[slots_all[:P]]).transpose(1, 0, 2)                # [Hkv][P][d]
+        Vp = load(vc[slots_all[:P]]).transpose(1, 0, 2)
         for r in range(R):
             bits = int(mask[b][r])
             win = [j for j in range(W) if (bits >> j) & 1]
-            Kw = widen(kc[slots_all[[P + j for j in win]]]).transpose(1, 0, 2) if win else np.zeros((Hkv, 0, d))
-            Vw = widen(vc[slots_all[[P + j for j in win]]]).transpose(1, 0, 2) if win else np.zeros((Hkv, 0, d))
+            Kw = load(kc[slots_all[[P + j for j in win]]]).transpose(1, 0, 2) if win else np.zeros((Hkv, 0, d))
+            Vw = load(vc[slots_all[[P + j for j in win]]]).transpose(1, 0, 2) if win else np.zeros((Hkv, 0, d))
             qv = widen(q[b * R + r])
             if not q_rotated:
                 qv = rnd(rope.rotate(qv, int(positions[b][r]), theta))
+            if q_fp8:
+                qv = decode_e4m3(encode_e4m3(qv))
             for kv in range(Hkv):
                 hs = slice(kv * g, (kv + 1) * g)
                 keys = np.concatenate([Kp[kv], Kw[kv]], axis=0)          # [P + |win|][d]

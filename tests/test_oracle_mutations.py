@@ -11,11 +11,13 @@ import pytest
 
 import oracle.attention as A
 import oracle.compact as C
+import oracle.fp8 as F8
 import oracle.merge as M
 import oracle.rope as R
 import oracle.tree as T
 import oracle.walk as W
 from tests import test_oracle_attention as PA
+from tests import test_oracle_fp8 as PF
 from tests import test_oracle_tree as PT
 from tests import test_oracle_walk_compact as PW
 from tests.conftest import load_golden
@@ -255,3 +257,64 @@ def test_sampling_mutations_caught(monkeypatch):
         monkeypatch.setattr(SM, name, bad)
         assert _fails(pin, *args), bad.__name__
         monkeypatch.undo()
+
+
+def _decode_bias8(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    v = np.where(e == 0, np.ldexp(m / 8.0, -7), np.ldexp(1.0 + m / 8.0, e - 8))
+    v = np.where(c & 0x80, -v, v)
+    return np.where((c & 0x7F) == 0x7F, np.nan, v)
+
+
+def _decode_ieee_specials(codes):  # exponent 15 reserved for inf/NaN, as in IEEE formats
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    v = _ORIG_DECODE(codes)
+    return np.where(((c >> 3) & 0xF) == 0xF, np.nan, v)
+
+
+def _decode_subnormal_no_scale(codes):  # subnormals read as 2^-7 * m / 8 (the normal formula with e = 0)
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    v = _ORIG_DECODE(codes)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    sub = np.where(c & 0x80, -1.0, 1.0) * np.ldexp(1.0 + m / 8.0, -7)
+    return np.where((e == 0) & (m != 0), sub, v)
+
+
+_ORIG_DECODE = F8.decode_e4m3
+_ORIG_ENCODE = F8.encode_e4m3
+
+
+def _encode_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    out = _ORIG_ENCODE(x)
+    grid = _ORIG_DECODE(np.arange(0x7F, dtype=np.uint8))
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(grid, a), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    tie = (a - grid[lo]) == (grid[hi] - a)
+    return np.where(tie & (a < 448), (hi | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8), out)
+
+
+def _encode_truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    grid = _ORIG_DECODE(np.arange(0x7F, dtype=np.uint8))
+    a = np.minimum(np.abs(x), 448.0)
+    code = np.clip(np.searchsorted(grid, a, side="right") - 1, 0, 0x7E)
+    return (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def _encode_nan_on_overflow(x):
+    x = np.asarray(x, dtype=np.float64)
+    return np.where(np.abs(x) >= 464, np.uint8(0x7F), _ORIG_ENCODE(x)).astype(np.uint8)
+
+
+def test_fp8_mutations_caught(monkeypatch):
+    for bad in (_decode_bias8, _decode_ieee_specials, _decode_subnormal_no_scale):
+        monkeypatch.setattr(F8, "decode_e4m3", bad)
+        assert _fails(PF.test_decode_fixed_points) or _fails(PF.test_decode_matches_torch_on_every_code)
+        monkeypatch.setattr(F8, "decode_e4m3", _ORIG_DECODE)
+    for bad in (_encode_ties_away, _encode_truncate, _encode_nan_on_overflow):
+        monkeypatch.setattr(F8, "encode_e4m3", bad)
+        assert _fails(PF.test_encode_matches_torch_below_saturation) or _fails(PF.test_encode_ties_to_even_and_saturates)
+        monkeypatch.setattr(F8, "encode_e4m3", _ORIG_ENCODE)

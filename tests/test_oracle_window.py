@@ -159,3 +159,57 @@ def test_window_order_is_irrelevant():
     masks2 = [sum(1 << int(perm[j]) for j in range(W) if (m >> j) & 1) for m in masks]
     out2, lse2 = A.window_attention(q, kc2, vc2, table, [P], [masks2], pos, W, Hkv, THETA, page_size=page)
     assert np.allclose(out, out2, atol=1e-12) and np.allclose(lse, lse2, atol=1e-12)
+
+
+def test_fp8_cache_reads_the_values_its_bytes_encode():
+    """kv_fp8: a cache of E4M3 bytes attends exactly like a bf16 cache holding
+    the same values (every E4M3 value is a bf16 value, so the bf16 cache is
+    exact). The bytes cover subnormals, both signs and the largest finite code;
+    a wrong decode, or K and V swapped, moves the result."""
+    from oracle import fp8 as F8
+    rng = np.random.default_rng(91)
+    B, R, W, Hq, Hkv, d, page = 2, 3, 5, 4, 2, 16, 4
+    P = [7, 0]
+    slots = 64
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F and (c & 0x7F) < 0x60], np.uint8)
+    k8 = rng.choice(finite, size=(slots, Hkv, d))
+    v8 = rng.choice(np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8), size=(slots, Hkv, d))
+    as_bf16 = lambda c: (F8.decode_e4m3(c).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert (A.widen(as_bf16(k8)) == F8.decode_e4m3(k8)).all()
+    table = rng.permutation(np.arange(1, 16, dtype=np.int32))[:6].reshape(B, 3)
+    q = (rng.normal(0, 0.3, (B * R, Hq, d)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    mask = [[int(x) for x in rng.integers(0, 1 << W, R)] for _ in range(B)]
+    pos = [[p + r for r in range(R)] for p in P]
+    args = (table, P, mask, pos, W, Hkv, THETA)
+    o8, l8 = A.window_attention(q, k8, v8, *args, page_size=page, kv_fp8=True)
+    ob, lb = A.window_attention(q, as_bf16(k8), as_bf16(v8), *args, page_size=page)
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
+    o_sw, _ = A.window_attention(q, v8, k8, *args, page_size=page, kv_fp8=True)
+    assert not np.allclose(o_sw, o8)
+
+
+def test_fp8_query_cast():
+    """q_fp8: a query whose values are already E4M3 values is left as it is
+    (the cast is exact there); any other query moves by at most one E4M3 step
+    per element, and so do the scores: the result changes, within that bound
+    on the log-sum-exp."""
+    from oracle import fp8 as F8
+    rng = np.random.default_rng(92)
+    B, R, W, Hq, Hkv, d, page = 1, 2, 3, 2, 1, 8, 4
+    k = rng.normal(0, 1, (32, Hkv, d))
+    v = rng.normal(0, 1, (32, Hkv, d))
+    table = np.array([[3, 5, 1]], np.int32)
+    args = (k, v, table, [6], [[5, 3]], [[0, 0]], W, Hkv, THETA)
+    q8 = F8.decode_e4m3(rng.integers(0, 0x60, (B * R, Hq, d)).astype(np.uint8))
+    o1, l1 = A.window_attention(q8, *args, page_size=page, q_rotated=True, q_fp8=True)
+    o0, l0 = A.window_attention(q8, *args, page_size=page, q_rotated=True)
+    assert np.array_equal(o1, o0) and np.array_equal(l1, l0)
+    q = rng.normal(0, 1, (B * R, Hq, d))
+    o1, l1 = A.window_attention(q, *args, page_size=page, q_rotated=True, q_fp8=True)
+    o0, l0 = A.window_attention(q, *args, page_size=page, q_rotated=True)
+    assert not np.allclose(l1, l0)
+    # |q8 - q| <= 2^-4 |q| elementwise, so each score moves by at most
+    # 2^-4 sum_i |q_i k_i| / sqrt(d), and the log-sum-exp by no more
+    bound = 2.0 ** -4 * np.abs(q[:, :, None, :] * k[None, :, 0, None, :].transpose(0, 2, 1, 3)).sum(-1).max() \
+        / math.sqrt(d) / math.log(2)
+    assert np.abs(l1 - l0).max() <= bound

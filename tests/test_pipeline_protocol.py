@@ -18,10 +18,15 @@ the condition under which the hardware's answer is the intended one. The
 model also tracks which buffers (Q tiles, ring slots) queued MMAs have still
 to read, and fails if a load lands in one of them first.
 
+With ``f8`` (an FP8 cache) two V-tile warps each widen half of every V
+tile's rows in place and both arrive on vready and win_bar (count 2); the
+tensor core must never read a V tile before both halves are widened.
+
 Mutants the model has to catch: V-tile warps that wait on a barrier shared by
 K and V loads (only for the V phases, or for every phase in order), a V slot
-released after the first row tile's PV instead of the last, and the Q tiles
-released after a segment's second S instead of its last.
+released after the first row tile's PV instead of the last, the Q tiles
+released after a segment's second S instead of its last, and (FP8) vready
+and win_bar left at count 1 for the two V warps.
 """
 import collections
 import random
@@ -61,7 +66,7 @@ def _kind_index(use, slots):
     return rnd if slots % 2 == 0 else rnd >> 1
 
 
-def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=600000):
+def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=600000, f8=False):
     """segs: (key tiles, row tiles present) per segment. Returns None when
     every role finishes, else the blocked waits; raises ProtocolError on an
     unsound step."""
@@ -73,14 +78,16 @@ def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=60000
         bars[name] = _Bar(name, count)
 
     for s in range(slots):
-        for n in ("full", "kfull", "vfull", "vready", "empty"):
+        for n in ("full", "kfull", "vfull", "empty"):
             bar(f"{n}{s}")
+        bar(f"vready{s}", 2 if f8 and mutant != "f8_count1" else 1)
     for t in range(2):
         bar(f"s_full{t}"), bar(f"p_full{t}", 128), bar(f"o_fin{t}"), bar(f"o_free{t}", 128)
-    bar("q_full"), bar("q_empty"), bar("win_bar")
+    bar("q_full"), bar("q_empty"), bar("win_bar", 2 if f8 and mutant != "f8_count1" else 1)
     tma = []                       # [delay, barrier, phase]
     tensor_q = []                  # the issuer's MMAs and commits, run in order
     reads = collections.Counter()  # buffers that queued MMAs have still to read
+    widened = collections.Counter()  # F8: V use -> halves widened
 
     def mma_op(*bufs):
         for b in bufs:
@@ -169,6 +176,9 @@ def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=60000
                     yield ("wait", f"full{vuse % slots}", vuse // slots)
                 else:
                     yield ("wait", f"vfull{vuse % slots}", _kind_index(vuse, slots))
+                if f8:
+                    yield ("step",)
+                    widened[vuse] += 1
                 bars[f"vready{vuse % slots}"].arrive(_kind_index(vuse, slots))
                 yield ("step",)
             for t in range(2):
@@ -197,6 +207,8 @@ def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=60000
             scnt += 1
 
     roles = {"prod": producer(), "mma": mma(), "vw": v_tile_warp(), "sm0": softmax(0), "sm1": softmax(1)}
+    if f8:
+        roles["vw1"] = v_tile_warp()
     pending = {k: None for k in roles}
     done = set()
     for _ in range(max_steps):
@@ -212,6 +224,8 @@ def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=60000
             else:
                 for b in op[1]:
                     reads[b] -= 1
+                    if f8 and b[0] == "kv" and b[1] % 2 == 1 and widened[b[1]] < 2:
+                        raise ProtocolError(f"MMA read V use {b[1]} before both halves were widened")
         ready = [k for k in roles if k not in done and (pending[k] is None or bars[pending[k][1]].passes(pending[k][2]))]
         if not ready:
             if not tma and not tensor_q:
@@ -219,6 +233,8 @@ def _simulate(segs, slots, seed, mutant=None, slow_v_warp=False, max_steps=60000
             continue
         if slow_v_warp and "vw" in ready and len(ready) > 1 and rng.random() < 0.9:
             ready.remove("vw")
+        if f8 and slow_v_warp and "vw1" in ready and len(ready) > 1 and rng.random() < 0.5:
+            ready.remove("vw1")
         k = rng.choice(ready)
         try:
             nxt = next(roles[k])
@@ -236,21 +252,23 @@ def _cases(n, seed0):
         yield segs, rng.choice([5, 8]), seed0 + i, i % 2 == 0
 
 
-def test_pipeline_never_deadlocks_and_waits_are_sound():
+@pytest.mark.parametrize("f8", [False, True])
+def test_pipeline_never_deadlocks_and_waits_are_sound(f8):
     stuck = [(segs, slots, seed) for segs, slots, seed, slow in _cases(120, 7000)
-             if _simulate(segs, slots, seed, None, slow) is not None]
+             if _simulate(segs, slots, seed, None, slow, f8=f8) is not None]
     assert not stuck, stuck[:3]
 
 
-@pytest.mark.parametrize("mutant", ["shared_v_only", "shared_all", "early_v_release", "early_q_release"])
-def test_model_catches_protocol_mutants(mutant):
+@pytest.mark.parametrize("mutant, f8", [("shared_v_only", False), ("shared_all", False), ("early_v_release", False),
+                                        ("early_q_release", False), ("f8_count1", True)])
+def test_model_catches_protocol_mutants(mutant, f8):
     """Each flawed protocol breaks on some schedule: an arrival for a phase
     the barrier is not in, a waiter two phases behind, a load over a buffer
-    still to be read, or a deadlock."""
+    still to be read, a K tile read before it is widened, or a deadlock."""
     caught = False
     for segs, slots, seed, slow in _cases(800, 9100):
         try:
-            caught = _simulate(segs, slots, seed, mutant, slow) is not None
+            caught = _simulate(segs, slots, seed, mutant, slow, f8=f8) is not None
         except ProtocolError:
             caught = True
         if caught:

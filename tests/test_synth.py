@@ -54,3 +54,20 @@ def test_bf16_rounding_is_nearest_even():
     x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 65504.0], np.float32)
     got = S.bf16_bits_to_f64(S.f32_to_bf16_bits(x))
     assert got.tolist() == [1.0, 1.0, 1.0 + 2 ** -6, -2.5, 65536.0]
+
+
+def test_e4m3_draws_are_finite_and_normal_shaped():
+    """normal_e4m3: no NaN code, both signs, and the decoded draws keep the
+    N(0,1) shape (each value is the draw with its mantissa cut to three bits,
+    so within 12.5% below it in magnitude)."""
+    from oracle import fp8 as F8
+    rng = np.random.default_rng(0)
+    codes = S.normal_e4m3(rng, (200000,))
+    assert ((codes & 0x7F) != 0x7F).all()
+    x = F8.decode_e4m3(codes)
+    assert abs(x.mean()) < 0.01 and 0.85 < x.std() < 1.0
+    assert (x > 0).mean() > 0.49 and (x < 0).mean() > 0.49
+    ref = np.random.default_rng(0).standard_normal(200000, dtype=np.float32).astype(np.float64)
+    big = np.abs(ref) >= 2.0 ** -6
+    assert (np.abs(x[big]) <= np.abs(ref[big])).all() and (np.abs(x[big]) > 0.875 * np.abs(ref[big])).all()
+    assert (x[~big] == 0).all()
