@@ -614,6 +614,7 @@ def time_fp8_attention(inp, db, stream, flush, args, hbm, tf_sus):
                 "frac": t_mma / t,
                 "peak_source": "measured sustained bf16 x 2 for the E4M3 half (S), x 1 for the f16 half (P V)"}
     roof["hbm_frac"] = t_hbm / t
+    roof["traffic_tree_pass"] = recorded_traffic("fp8:" + w.name)
     return {"workload": w.name, "kv_dtype": "e4m3 (unscaled)",
             "compute": "S: E4M3 MMA (query cast to E4M3); P V: f16 MMA (V widened); fp32 accumulation",
             "us": us, "rows_per_s": BN / t, "bytes": nbytes, "flops": flops, "roofline": roof, "reps": reps}
