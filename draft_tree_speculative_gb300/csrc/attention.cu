@@ -1143,13 +1143,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
+// L2 promotion: 256-byte fetches suit rows of 256 bytes or more; a 128-byte
+// row (one KV head of an E4M3 cache) takes 128-byte fetches, so that a fetch
+// does not also bring in the next head's row, which another CTA reads later.
 bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-            const cuuint32_t *box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+            const cuuint32_t *box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+            CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   auto enc = get_encode_fn();
   if (enc == nullptr) return false;
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -1162,7 +1166,8 @@ bool make_cache_map(CUtensorMap *map, const void *base, int d, int Hkv, int64_t 
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_slots)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(Hkv) * d * esz};
   cuuint32_t box[3] = {f8 ? 128u : 64u, 1, static_cast<cuuint32_t>(rows_per_box)};
-  return encode(map, base, 3, dims, strides, box, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  return encode(map, base, 3, dims, strides, box, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                f8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // 4-D view (d, g, Hkv, B*N) of the queries [B*N][Hq][d]; box (64, g, 1, npt)
