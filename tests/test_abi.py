@@ -86,3 +86,30 @@ def test_argmax_host_checks(lib):
                                            0, None, None) == dts.ERR_UNSUPPORTED
     assert L.dts_verify_tree_greedy_logits(None, None, 10, 10, None, None, None, 2, 8, None, None, None, None, None,
                                            0, None, None) == dts.ERR_INVALID
+
+
+def test_fp8_host_checks(lib):
+    """The E4M3-cache calls take d = 128 only and otherwise validate like the
+    bf16 calls, all before any launch."""
+    L = dts.lib()
+    wkv = lambda d, B=1, ps=64, ptr=None: L.dts_write_window_kv_fp8(ptr, ptr, ptr, ptr, 4, ps, ptr, B, 8, 8, d, 100,
+                                                                    5e5, ptr, ptr, None, None, None)
+    assert wkv(64) == dts.ERR_UNSUPPORTED            # the bf16 call takes d = 64; the E4M3 one does not
+    assert wkv(96) == dts.ERR_UNSUPPORTED
+    assert wkv(128, ps=48) == dts.ERR_UNSUPPORTED
+    assert wkv(128, B=0) == dts.OK
+    assert wkv(128) == dts.ERR_INVALID               # null pointers
+    att = lambda d, B=1, ps=64, hq=32: L.dts_tree_verify_attention_fp8(None, None, None, 100, None, 4, ps, None, 0,
+                                                                      None, None, 5e5, B, 8, hq, 8, d, 0.0, None,
+                                                                      None, None, 0, None, None)
+    assert att(64) == dts.ERR_UNSUPPORTED
+    assert att(128, ps=48) == dts.ERR_UNSUPPORTED
+    assert att(128, hq=30) == dts.ERR_INVALID        # Hq % Hkv != 0
+    assert att(128, B=0) == dts.OK
+    assert att(128) == dts.ERR_INVALID               # null pointers
+    win = lambda d, R=8, W=48: L.dts_tree_window_attention_fp8(None, None, None, 100, None, 4, 64, None, 0, None,
+                                                              None, 5e5, 1, R, W, 32, 8, d, 0.0, None, None, None,
+                                                              0, None, None)
+    assert win(64) == dts.ERR_UNSUPPORTED
+    assert win(128, W=65) == dts.ERR_UNSUPPORTED
+    assert win(128) == dts.ERR_INVALID
