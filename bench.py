@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-argmax", action="store_true", help="skip the target-argmax measurement")
     ap.add_argument("--no-lanes", action="store_true", help="skip the draft-lane attention measurement")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-KV attention measurement")
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="skip the long-context and high-concurrency workloads' measurements")
     return ap.parse_args()
 
 
@@ -73,6 +75,30 @@ def attention_work(inp: synth.VerifyInputs):
     depth_sum = int(inp.depth.sum()) + w.B * w.N
     flops = 4 * w.N * w.Hq * w.d * int(P.sum()) + 4 * w.Hq * w.d * depth_sum
     return bytes_, flops
+
+
+def attention_roofline(inp, attn_ms, workload):
+    """Roofline of one tree_verify_attention call (prep, tree pass, merge) of
+    mean CUDA-event duration attn_ms: the slower of the algorithmic bytes at the
+    measured HBM bandwidth and the algorithmic FLOPs at the measured sustained
+    bf16 rate (the call runs inside a long step)."""
+    bytes_, flops = attention_work(inp)
+    hbm, tf_burst, tf_sus, src = load_peaks()
+    t_hbm = bytes_ / (hbm * 1e9)
+    t_mma = flops / (tf_sus * 1e12)
+    if t_hbm >= t_mma:
+        roof = {"bound": "hbm", "achieved": bytes_ / (attn_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (attn_ms / 1e3) / 1e12, "peak": tf_sus, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(workload)
+    roof["kernel"] = "tree_verify_attention (attn_prep_kernel + tree_prefix_kernel + tree_merge_kernel)"
+    roof["algorithmic_bytes"] = bytes_
+    roof["algorithmic_flops"] = flops
+    roof["peak_source"] = f"{src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})"
+    roof["roofline_us"] = max(t_hbm, t_mma) * 1e6
+    roof["attention_us"] = attn_ms * 1e3
+    return roof
 
 
 def load_peaks():
@@ -256,7 +282,10 @@ def oracle_sample(inp: synth.VerifyInputs, b: int, nodes):
     return len(nodes)
 
 
-def cpu_rows_per_s(inp, steps=1, nodes_per_step=8, min_seconds=0.0, max_steps=100000):
+ORACLE_ROWS_PER_SAMPLE = 16  # verify rows (all heads) of one request per oracle sample, in both oracle legs
+
+
+def cpu_rows_per_s(inp, steps=1, nodes_per_step=ORACLE_ROWS_PER_SAMPLE, min_seconds=0.0, max_steps=100000):
     """The oracle over `steps` samples (or, with min_seconds, as many as fit in
     that time, at most max_steps); each sample is `nodes_per_step` verify rows
     of one request (requests in turn) plus that request's walk and compaction."""
@@ -339,22 +368,8 @@ def run_ours(args, rank, world, local_rank):
 
     # roofline of the attention call (prep, tree pass, merge)
     attn_ms = statistics.mean(per_call["attention"])
-    bytes_, flops = attention_work(inp)
     hbm, tf_burst, tf_sus, src = load_peaks()
-    t_hbm = bytes_ / (hbm * 1e9)
-    t_mma = flops / (tf_sus * 1e12)
-    if t_hbm >= t_mma:
-        roof = {"bound": "hbm", "achieved": bytes_ / (attn_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops / (attn_ms / 1e3) / 1e12, "peak": tf_sus, "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(args.workload)
-    roof["kernel"] = "tree_verify_attention (attn_prep_kernel + tree_prefix_kernel + tree_merge_kernel)"
-    roof["algorithmic_bytes"] = bytes_
-    roof["algorithmic_flops"] = flops
-    roof["peak_source"] = f"{src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})"
-    roof["roofline_us"] = max(t_hbm, t_mma) * 1e6
-    roof["attention_us"] = attn_ms * 1e3
+    roof = attention_roofline(inp, attn_ms, args.workload)
 
     # end to end through the public API: pinned host inputs in, result out.
     # A serving loop overlaps the next step's upload with this step's compute:
@@ -435,15 +450,93 @@ def run_ours(args, rank, world, local_rank):
         line["lane_attention"] = time_lane_attention(stream, flush, args, hbm, tf_sus, db.device)
     if not args.no_fp8:
         line["fp8_attention"] = time_fp8_attention(inp, db, stream, flush, args, hbm, tf_sus)
+    if not args.no_side_workloads:
+        line["workloads"] = {}
+        for name in SIDE_WORKLOADS:
+            if name != w.name:
+                line["workloads"][name] = time_side_workload(name, args, dev, stream, flush)
     clocks = clk.summary()
     if clocks is not None:
         line["clocks"] = clocks
     if rank == 0 and not args.no_cpu_baseline:
         # about 12 s of oracle work on the host cores
-        v, dt, sample = cpu_rows_per_s(inp, steps=1, nodes_per_step=min(16, w.N), min_seconds=12.0)
+        v, dt, sample = cpu_rows_per_s(inp, steps=1, min_seconds=12.0)
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle",
                                 "sample": sample, "seconds": dt}
     return line
+
+
+SIDE_WORKLOADS = ("longctx_p131072_n64", "highconc_b128_n16")
+
+
+def time_side_workload(name, args, dev, stream, flush):
+    """One more workload's verify step, timed in the same run as the headline:
+    per-call CUDA events over `reps` steps, L2 flushed before each step. The
+    attention call gets its roofline (HBM or sustained tensor, whichever
+    bounds it). A workload with fp8 layers (the high-concurrency batch) runs
+    the full verify step: mask, window K/V, attention, the target argmax over
+    its fp32 logits fed straight into the walk (dts_verify_tree_greedy_logits),
+    then the compaction of every K/V buffer (the attention layer's bf16 K and V
+    plus 2 x fp8_layers fp8 buffers) and of the hidden rows."""
+    import torch
+    from draft_tree_speculative_gb300 import target_argmax_workspace, verify_tree_greedy_logits
+    from draft_tree_speculative_gb300.step import DeviceBatch
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    db = DeviceBatch(inp, device=dev)
+    full = w.fp8_layers > 0
+    names = ["mask", "window_kv", "attention", "walk", "compact"]
+    calls = [db.mask_step, db.window_kv_step, db.attention_step, db.walk_step, db.compact_step]
+    logits = ws = arg = None
+    if full:
+        logits = torch.from_numpy(synth.target_logits(w, inp.target_argmax)).to(dev)
+        arg = torch.empty((w.B, w.N), dtype=torch.int32, device=dev)
+        ws = torch.empty(max(8, target_argmax_workspace(w.B * w.N, w.vocab)), dtype=torch.uint8, device=dev)
+        names[3] = "argmax_walk"
+        calls[3] = lambda st: verify_tree_greedy_logits(db.draft, logits, arg, db.accept_len, db.accepted_path,
+                                                         db.accepted_tokens, ws, parents=db.parents, err=db.err,
+                                                         stream=st)
+    reps = max(5, min(args.steps, 30))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.fill_(1)
+            for c in calls:
+                c(stream)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            for e in ev:
+                flush.fill_(1)
+                for k, c in enumerate(calls):
+                    e[k].record(stream)
+                    c(stream)
+                e[-1].record(stream)
+        torch.cuda.synchronize()
+    check_device_error(db, f"the {name} steps")
+    per = {n: [e[k].elapsed_time(e[k + 1]) for e in ev] for k, n in enumerate(names)}
+    step_us = statistics.median(e[0].elapsed_time(e[-1]) for e in ev) * 1e3
+    attn_ms = statistics.mean(per["attention"])
+    roof = attention_roofline(inp, attn_ms, name)
+    out = {"B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "prefix_len_max": int(inp.vc.max()),
+           "prefix_len_sum": int(inp.vc.sum()), "reps": reps,
+           "attention_us": attn_ms * 1e3, "rows_per_s": w.B * w.N / (attn_ms / 1e3), "roofline": roof,
+           "kernels_us": {n: statistics.median(v) * 1e3 for n, v in per.items()}}
+    clocks = clk.summary()
+    if clocks is not None:
+        out["clocks"] = clocks
+    if full:
+        out["full_step_us"] = step_us
+        out["full_step"] = ("mask, window K/V, attention, target argmax over fp32 logits "
+                            f"[{w.B * w.N}][{w.vocab}] + walk, compaction of {len(db.kv_entries)} K/V buffers "
+                            f"({2 * w.fp8_layers} fp8 layers' K and V plus the bf16 attention layer) and hidden rows "
+                            f"[{w.B * w.N}][{inp.hidden.shape[1]}]")
+        out["argmax_matches_planted_target"] = bool((arg.cpu().numpy() == inp.target_argmax).all())
+    else:
+        out["step_us"] = step_us
+    del db, logits, ws, arg
+    torch.cuda.empty_cache()
+    return out
 
 
 def time_target_argmax(inp, db, stream, flush, args, hbm):
@@ -623,8 +716,8 @@ def time_fp8_attention(inp, db, stream, flush, args, hbm, tf_sus):
 def run_reference(args):
     w = synth.WORKLOADS[args.workload]
     inp = synth.make_inputs(w)
-    cpu_rows_per_s(inp, steps=args.warmup, nodes_per_step=2)
-    v, dt, sample = cpu_rows_per_s(inp, steps=args.steps, nodes_per_step=2)
+    cpu_rows_per_s(inp, steps=args.warmup)
+    v, dt, sample = cpu_rows_per_s(inp, steps=args.steps)
     line = {
         "metric": METRIC, "value": v, "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",

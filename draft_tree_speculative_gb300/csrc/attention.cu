@@ -1415,11 +1415,41 @@ __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_ws_mutex;
-void *g_static_ws_ptr[kMaxDevices] = {};
+struct StaticWsEntry {
+  unsigned long long ctx_id;  // the context the address belongs to
+  void *ptr;
+};
+StaticWsEntry g_static_ws[kMaxDevices] = {};
 
-// Device address of g_static_workspace on the current device. The host-side
-// name of the array is only a stand-in; its device address has to be asked
-// for once per device, with that device current.
+// Identity of the calling thread's current context. A device reset ends the
+// primary context and a later call runs in a new one, with a new id, where the
+// array has been loaded again at a possibly different address.
+bool current_context_id(unsigned long long *id) {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+    return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_static_workspace in the current device's context. The
+// host-side name of the array is only a stand-in; its device address has to
+// be asked for once per device and context, with that device current.
 void *static_workspace(int *status) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -1427,16 +1457,22 @@ void *static_workspace(int *status) {
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(g_static_ws_mutex);
-  if (g_static_ws_ptr[dev] == nullptr) {
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
+  StaticWsEntry &e = g_static_ws[dev];
+  if (e.ptr == nullptr || !have_ctx || e.ctx_id != ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) {
       *status = DTS_ERR_CUDA;
       return nullptr;
     }
-    g_static_ws_ptr[dev] = p;
+    // the lookup creates the context if there was none yet: key the entry on it
+    unsigned long long ctx_after = 0;
+    e.ptr = p;
+    e.ctx_id = current_context_id(&ctx_after) ? ctx_after : 0;
   }
   *status = DTS_OK;
-  return g_static_ws_ptr[dev];
+  return e.ptr;
 }
 
 }  // namespace
@@ -1449,9 +1485,16 @@ extern "C" int dts_tree_verify_attention_static_ws(const uint16_t *q, const uint
                                                    int B, int N, int Hq, int Hkv, int d, float softmax_scale,
                                                    uint16_t *out, float *lse2, int32_t *err_dev,
                                                    dts_stream_t stream) {
-  if (B == 0) return DTS_OK;
-  const size_t need = dts_tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_prefix);
-  if (need > kStaticWorkspaceBytes) return DTS_ERR_WORKSPACE;
+  // Shapes, pointers and B = 0 are checked by the regular entry point, so
+  // both calls answer the same arguments alike. Given no workspace it launches
+  // nothing and returns the argument error, DTS_OK for B = 0, or (arguments
+  // valid) DTS_ERR_WORKSPACE; only then is the static array looked up.
+  const int checked = dts_tree_verify_attention(q, k_cache, v_cache, num_slots, page_table, max_pages, page_size,
+                                                prefix_len, max_prefix, mask, positions, rope_theta, B, N, Hq, Hkv,
+                                                d, softmax_scale, out, lse2, nullptr, 0, err_dev, stream);
+  if (checked != DTS_ERR_WORKSPACE) return checked;
+  if (dts_tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_prefix) > kStaticWorkspaceBytes)
+    return DTS_ERR_WORKSPACE;
   int status = DTS_OK;
   void *ws = static_workspace(&status);
   if (ws == nullptr) return status;

@@ -305,9 +305,14 @@ int dts_tree_verify_attention_fp8(const uint16_t *q, const uint8_t *k_cache,
  * process exits. Shapes whose workspace (dts_tree_verify_attention_workspace)
  * exceeds 64 MiB get DTS_ERR_WORKSPACE and nothing runs.
  *
+ * Arguments are validated exactly as dts_tree_verify_attention validates
+ * them (B = 0 returns DTS_OK), before the array is touched.
+ *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call before any stream capture. The call allocates and frees nothing.
+ * (cudaGetSymbolAddress, with that device current) and keeps it, keyed by the
+ * current context: after a device reset the next call looks it up again in
+ * the new context. Make the first call on a device (and the first after a
+ * reset) before any stream capture. The call allocates and frees nothing.
  * All calls share the one array: calls whose work overlaps on the GPU (other
  * streams, other host threads) race and give wrong results, so serialise them.
  * Nothing in the array needs clearing between calls.

@@ -113,3 +113,29 @@ def test_fp8_host_checks(lib):
     assert win(64) == dts.ERR_UNSUPPORTED
     assert win(128, W=65) == dts.ERR_UNSUPPORTED
     assert win(128) == dts.ERR_INVALID
+
+
+def test_static_workspace_validates_like_the_regular_call(lib):
+    """The allocation-free attention answers every argument error exactly as
+    dts_tree_verify_attention does (same checks, same order), B = 0 included,
+    without touching the device: nothing is looked up or launched."""
+    L = dts.lib()
+
+    def both(B=1, N=8, Hq=32, Hkv=8, d=128, ps=64, theta=5e5, ptr=None):
+        reg = L.dts_tree_verify_attention(ptr, ptr, ptr, 100, ptr, 4, ps, ptr, 0, ptr, ptr, theta, B, N, Hq, Hkv, d,
+                                          0.0, ptr, ptr, None, 0, None, None)
+        sta = L.dts_tree_verify_attention_static_ws(ptr, ptr, ptr, 100, ptr, 4, ps, ptr, 0, ptr, ptr, theta, B, N,
+                                                    Hq, Hkv, d, 0.0, ptr, ptr, None, None)
+        return reg, sta
+
+    for kw, want in [(dict(B=0), dts.OK), (dict(B=0, N=65), dts.ERR_UNSUPPORTED), (dict(N=65), dts.ERR_UNSUPPORTED),
+                     (dict(d=96), dts.ERR_UNSUPPORTED), (dict(ps=48), dts.ERR_UNSUPPORTED),
+                     (dict(Hq=30), dts.ERR_INVALID), (dict(theta=0.0, ptr=4096), dts.ERR_INVALID),
+                     (dict(B=-1), dts.ERR_INVALID), (dict(), dts.ERR_INVALID)]:
+        reg, sta = both(**kw)
+        assert reg == sta == want, (kw, reg, sta)
+    # a shape beyond the static array is refused as a workspace error once the
+    # arguments are valid (aligned non-null pointers; nothing is launched)
+    big = dict(B=32, N=64, ptr=4096)
+    assert dts.tree_verify_attention_workspace(32, 64, 32, 8, 128, 0) > (64 << 20)
+    assert both(**big) == (dts.ERR_WORKSPACE, dts.ERR_WORKSPACE)
