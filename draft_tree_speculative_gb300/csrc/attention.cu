@@ -207,9 +207,9 @@ struct PrefixShape {
   static constexpr uint32_t kBlockBytes = 128 * 128;   // one 64-column block of a 128-row tile
   static constexpr int kSlots = D == 128 ? 5 : 8;      // K/V ring
   static constexpr uint32_t kBarBytes = 512;
-  // kfull, vfull, empty, vready rings, 12 single barriers, two poison masks,
+  // kfull, vfull, empty, vready rings, 10 single barriers, two poison masks,
   // the tile total (two words) and the TMEM address / abort flag words
-  static_assert((4 * kSlots + 12) * 8 + 16 + 16 + 8 <= kBarBytes, "barrier area too small");
+  static_assert((4 * kSlots + 10) * 8 + 16 + 16 + 8 <= kBarBytes, "barrier area too small");
   static constexpr uint32_t kSmem = 1024 /*align*/ + 2 * kTileBytes + kSlots * kTileBytes + kBarBytes;
 };
 
@@ -277,6 +277,21 @@ __device__ __forceinline__ uint32_t visible_word(int o, uint64_t mrow) {
   if (o >= 64) return 0u;
   if (o >= 0) return static_cast<uint32_t>(mrow >> o);
   return static_cast<uint32_t>(mrow << -o) | ((1u << -o) - 1u);
+}
+
+// P_t(r), the r-th key tile's P of row tile t (counted over the CTA's
+// segments), passes from softmax group t to the MMA warp through a named
+// barrier: the group's 128 threads arrive, the MMA warp syncs. Rounds r and
+// r + 1 use different barriers, so a group that gives up can always arrive
+// once more for the round the MMA warp may be waiting for (see the softmax
+// groups) without landing in the round before it.
+// Row tile 0's rounds also take warp 3, which vouches that V(j) is clean and
+// K(j + 1) has landed before the MMA warp issues PV_0(j) and S_0(j + 1).
+constexpr uint32_t kP0Threads = 128 + 32 + 32;
+constexpr uint32_t kP1Threads = 128 + 32;
+__device__ __forceinline__ uint32_t p_bar_threads(int t) { return t == 0 ? kP0Threads : kP1Threads; }
+__device__ __forceinline__ uint32_t p_bar_id(int t, int r) {
+  return 1u + 2u * static_cast<uint32_t>(t) + (static_cast<uint32_t>(r) & 1u);
 }
 
 // Phase of use u on a barrier that only the slot's uses of u's kind (K: even
@@ -436,8 +451,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t *vfull = bars + kSlots;
   uint64_t *empty = bars + 2 * kSlots;
   uint64_t *s_full = bars + 3 * kSlots;
-  uint64_t *p_full = s_full + 2;
-  uint64_t *o_fin = p_full + 2;
+  uint64_t *o_fin = s_full + 2;
   uint64_t *o_free = o_fin + 2;
   uint64_t *q_full = o_free + 2;
   uint64_t *q_empty = q_full + 1;
@@ -457,7 +471,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
       mbar_init(&o_fin[t], 1);
       mbar_init(&o_free[t], 128);
     }
@@ -513,9 +526,11 @@ __global__ void __launch_bounds__(384, 1)
   Segment sg;
 
   // Register split: the control warpgroup (TMA, MMA) gives registers to the
-  // two softmax groups. 128 * 96 + 256 * 200 = 384 * 168, the launch budget.
+  // two softmax groups: 128 * 112 + 256 * 192 = 63 488 <= 384 * 168, the
+  // launch budget. Below 112 the control roles' loops spill to local memory,
+  // which every barrier wait of the MMA warp then pays for.
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory");
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer
       // The whole warp walks the tiles; page ids come 32 at a time (one
@@ -640,7 +655,8 @@ __global__ void __launch_bounds__(384, 1)
           mma_ts(d_tmem, p_tmem + ks * 8, vb + static_cast<uint64_t>(ks) * (2048 >> 4), kIdescO, ks == 0 ? acc0 : 1u);
       };
       int use = 0, segc = 0;
-      int tcnt[2] = {0, 0}, scnt[2] = {0, 0};
+      int tcnt[2] = {0, 0};
+      int p0_rounds = 0;  // rounds of row tile 0 this warp has synced
       bool ok = true;
       while (ok && walker.next(a, sg)) {
         const int nkt = sg.lt1 - sg.lt0;
@@ -650,80 +666,97 @@ __global__ void __launch_bounds__(384, 1)
              mbar_wait(&kfull[slot_of(use)], kind_phase_of(use), abort_flag);
         if (!ok) break;
         tc_fence_after();
+        int kslot = slot_of(use);  // the slot of K(j + 1) in the loop below, of K(0) here
         if (lane == 0) {
           // (row-tile loops run over the constant 2 so that per-tile counters
           // stay in registers)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t < nt) {
-              issue_s(t, slot_of(use));
+              issue_s(t, kslot);
               mma_commit(&s_full[t]);
             }
           }
           if (nkt == 1) mma_commit(q_empty);  // the segment's last S reads Q
-          mma_commit(&empty[slot_of(use)]);
+          mma_commit(&empty[kslot]);
         }
         __syncwarp();
-        // The tensor core takes about one group of MMAs at a time, so any work
-        // between two issue calls leaves it idle. Per row tile all waits come
-        // first; then PV_t(j) and S_t(j+1) go out back to back from one lane.
+        int vslot = kslot + 1 == kSlots ? 0 : kslot + 1;  // V(j)
+        // The tensor core takes about one MMA at a time from the issuing
+        // thread, so whatever that thread does between two groups leaves it
+        // idle; an mbarrier wait costs it ~135 cycles even on a completed
+        // phase, a named-barrier sync ~15. So the one wait per row tile and
+        // key tile is a named-barrier sync, after which PV_t(j) and S_t(j+1)
+        // go out back to back from one lane, and the abort flag read before
+        // them is looked at only after them.
         for (int j = 0; j < nkt && ok; ++j) {
-          const int vuse = use + 2 * j + 1;
-          const int vslot = slot_of(vuse);
-          const int kuse = use + 2 * (j + 1);
+          kslot = vslot + 1 == kSlots ? 0 : vslot + 1;  // K(j + 1)
           const bool more = j + 1 < nkt;
-          ok = mbar_wait(&vready[vslot], kind_phase_of(vuse), abort_flag) &&
-               (!more || mbar_wait(&kfull[slot_of(kuse)], kind_phase_of(kuse), abort_flag));
-          if (!ok) break;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t >= nt) break;
-            ok = mbar_wait(&p_full[t], static_cast<uint32_t>(tcnt[t] + j) & 1u, abort_flag);
-            // the first PV of a segment overwrites O: the previous epilogue must have read it
-            if (ok && j == 0 && scnt[t] > 0)
-              ok = mbar_wait(&o_free[t], static_cast<uint32_t>(scnt[t] - 1) & 1u, abort_flag);
-            if (!ok) break;
+            // Group t has stored P_t(j) in TMEM and, on a segment's first
+            // tile, read O_t of the previous segment (which PV_t(0)
+            // overwrites). In row tile 0's rounds warp 3 vouches for V(j)
+            // and K(j + 1). A warp that gives up sets the abort flag before
+            // its last arrival.
+            named_sync(p_bar_id(t, tcnt[t] + j), p_bar_threads(t));
+            if (t == 0) ++p0_rounds;
+            const int aborted = *abort_flag;
             tc_fence_after();
             if (lane == 0) {
               issue_pv(t, vslot, j == 0);
-              if (more) issue_s(t, slot_of(kuse));  // overwrites P_t(j) only after PV_t(j) read it
+              if (more) issue_s(t, kslot);  // overwrites P_t(j) only after PV_t(j) read it
               if (t == nt - 1) mma_commit(&empty[vslot]);
               if (more) {
                 mma_commit(&s_full[t]);
                 if (t == nt - 1) {
                   if (j + 2 == nkt) mma_commit(q_empty);
-                  mma_commit(&empty[slot_of(kuse)]);
+                  mma_commit(&empty[kslot]);
                 }
               } else {
                 mma_commit(&o_fin[t]);
               }
             }
             __syncwarp();
+            if (aborted) {
+              ok = false;
+              break;
+            }
           }
+          vslot = kslot + 1 == kSlots ? 0 : kslot + 1;  // V(j + 1)
         }
         use += 2 * nkt;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t < nt) {
-            tcnt[t] += nkt;
-            scnt[t] += 1;
-          }
-        }
+        for (int t = 0; t < 2; ++t)
+          if (t < nt) tcnt[t] += nkt;
         ++segc;
       }
-      if (!ok) dts::report(a.err, DTS_DEV_TIMEOUT);
+      if (!ok) {
+        // warp 3 may be blocked in row tile 0's round p0_rounds, which this
+        // warp has not joined; the abort flag is set, so one more arrival
+        // ends that sync and warp 3 stops there
+        named_arrive(p_bar_id(0, p0_rounds), kP0Threads);
+        dts::report(a.err, DTS_DEV_TIMEOUT);
+      }
       // drain: wait for every MMA issued so far before TMEM is released
       if (lane == 0) mma_commit(drain);
       __syncwarp();
       mbar_wait(drain, 0, abort_flag);
-    } else if (warp == 2 || (F8 && warp == 3)) {
-      // ---------------------------------------------------------- V-tile warp(s)
-      // Hands every V tile to the MMA warp (vready) once it has landed, after
-      // cleaning the ones that reach the window (clean_window_v), and
-      // publishes each segment's poisoned window keys (win_bar). F8: warps 2
-      // and 3 each widen half of every V tile's rows and publish their own mask.
+    } else {
+      // ---------------------------------------------------------- V-tile warp(s), voucher
+      // Warp 2 (and warp 3 under F8) hands every V tile on (vready) once it
+      // has landed, after cleaning the ones that reach the window
+      // (clean_window_v), and publishes each segment's poisoned window keys
+      // (win_bar). F8: warps 2 and 3 each widen half of every V tile's rows
+      // and publish their own mask. Warp 3 also vouches, in row tile 0's
+      // round j, that V(j) is ready and K(j + 1) has landed, so that the MMA
+      // warp waits only on the named barrier.
+      const bool v_role = warp == 2 || F8;
+      const bool voucher = warp == 3;
       const int vw = warp - 2;
       int use = 0, prev_nt = 0;
+      int rounds = 0;        // row tile 0 rounds this warp has synced (voucher)
       int scnt[2] = {0, 0};  // segments each softmax group has taken part in
       bool ok = true;
       while (ok && walker.next(a, sg)) {
@@ -732,39 +765,60 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < nkt && ok; ++j) {
           const int vuse = use + 2 * j + 1;
           const int vslot = vuse % kSlots;
-          ok = mbar_wait(&vfull[vslot], kind_phase<kSlots>(vuse), abort_flag);
-          if (!ok) break;
-          const int kbase = (sg.lt0 + j) * 128;
-          if constexpr (F8) {
-            seg_poison |= widen_fp8_v_rows(sKV + vslot * kTileBytes, vw * 64, min(128, sg.P + a.W - kbase),
-                                           kbase - sg.P, kbase + 128 > sg.P, lane);
-          } else if (kbase + 128 > sg.P) {  // the window's tiles (and the unit's end)
-            seg_poison |= clean_window_v<D>(sKV + vslot * kTileBytes, kbase - sg.P, a.W, lane);
+          if (v_role) {
+            ok = mbar_wait(&vfull[vslot], kind_phase<kSlots>(vuse), abort_flag);
+            if (!ok) break;
+            const int kbase = (sg.lt0 + j) * 128;
+            if constexpr (F8) {
+              seg_poison |= widen_fp8_v_rows(sKV + vslot * kTileBytes, vw * 64, min(128, sg.P + a.W - kbase),
+                                             kbase - sg.P, kbase + 128 > sg.P, lane);
+            } else if (kbase + 128 > sg.P) {  // the window's tiles (and the unit's end)
+              seg_poison |= clean_window_v<D>(sKV + vslot * kTileBytes, kbase - sg.P, a.W, lane);
+            }
+            if (lane == 0) mbar_arrive(&vready[vslot]);
+            __syncwarp();
           }
-          if (lane == 0) mbar_arrive(&vready[vslot]);
+          if (voucher) {
+            const int kuse = vuse + 1;
+            ok = mbar_wait(&vready[vslot], kind_phase<kSlots>(vuse), abort_flag) &&
+                 (j + 1 == nkt || mbar_wait(&kfull[kuse % kSlots], kind_phase<kSlots>(kuse), abort_flag));
+            if (!ok) break;
+            named_sync(p_bar_id(0, rounds), kP0Threads);
+            ++rounds;
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (v_role) {
+          // The groups that read the previous segment's mask must be past it
+          // (o_free follows their read) before it is overwritten.
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (ok && t < prev_nt && scnt[t] > 0)
+              ok = mbar_wait(&o_free[t], static_cast<uint32_t>(scnt[t] - 1) & 1u, abort_flag);
+          prev_nt = sg.nt;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (t < sg.nt) ++scnt[t];
+          if (lane == 0) {
+            poison[vw] = seg_poison;
+            mbar_arrive(win_bar);
+          }
           __syncwarp();
         }
-        // The groups that read the previous segment's mask must be past it
-        // (o_free follows their read) before it is overwritten.
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (ok && t < prev_nt && scnt[t] > 0)
-            ok = mbar_wait(&o_free[t], static_cast<uint32_t>(scnt[t] - 1) & 1u, abort_flag);
-        prev_nt = sg.nt;
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (t < sg.nt) ++scnt[t];
-        if (lane == 0) {
-          poison[vw] = seg_poison;
-          mbar_arrive(win_bar);
-        }
-        __syncwarp();
         use += 2 * nkt;
       }
-      if (!ok) dts::report(a.err, DTS_DEV_TIMEOUT);
+      if (!ok) {
+        // the MMA warp may be blocked in row tile 0's round `rounds`: one
+        // more arrival (the abort flag is set) ends it there
+        if (voucher) named_arrive(p_bar_id(0, rounds), kP0Threads);
+        dts::report(a.err, DTS_DEV_TIMEOUT);
+      }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
     // ------------------------------------------------------------ softmax groups
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;
@@ -774,6 +828,7 @@ __global__ void __launch_bounds__(384, 1)
     const float c = a.scale_log2;
     const uint64_t node_bits = a.W < 64 ? (1ull << a.W) - 1ull : ~0ull;  // the window's keys
     int tcnt = 0, scnt = 0, wcnt = 0;
+    int arrived = 0;  // this warp's arrivals on the P barriers: the next round is `arrived`
     bool ok = true;
     while (ok && walker.next(a, sg)) {
       const uint32_t wpar = static_cast<uint32_t>(wcnt++) & 1u;  // win_bar completes once per segment
@@ -884,7 +939,8 @@ __global__ void __launch_bounds__(384, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(&p_full[t]);
+        named_arrive(p_bar_id(t, arrived), p_bar_threads(t));
+        ++arrived;
       }
       if (!ok || !mbar_wait(&o_fin[t], static_cast<uint32_t>(scnt) & 1u, abort_flag) ||
           !mbar_wait(win_bar, wpar, abort_flag)) {
@@ -958,7 +1014,16 @@ __global__ void __launch_bounds__(384, 1)
       tcnt += nkt;
       ++scnt;
     }
-    if (!ok) dts::report(a.err, DTS_DEV_TIMEOUT);
+    if (!ok) {
+      // The MMA warp may be blocked in the sync of round `arrived`, which
+      // this warp has not joined. The abort flag is already set (by this
+      // warp's timeout or by the role whose flag made the wait give up), so
+      // one more arrival ends that sync and the MMA warp stops there. Round
+      // arrived - 1 went to the other barrier, so this arrival cannot land
+      // in it.
+      named_arrive(p_bar_id(t, arrived), p_bar_threads(t));
+      dts::report(a.err, DTS_DEV_TIMEOUT);
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -64,6 +64,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// ---------------------------------------------------------------- named barriers
+// Hardware barrier `id` (1..15; 0 is __syncthreads) over `count` threads, a
+// multiple of 32, every taking part warp with all its lanes. An arrival does
+// not block; a sync arrives and blocks until the round completes. A round
+// completes when `count` threads have arrived, so no warp may arrive twice
+// in one round. Unlike an mbarrier wait there is no time limit: a protocol
+// that syncs on one must guarantee the arrivals, aborts included.
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA / proxies
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
                                             uint64_t *bar) {
