@@ -143,6 +143,22 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, page_table, prefix_len, 
     return out, lse2
 
 
+def prefix_query(qv, q_fp8: bool):
+    """The query the prefix keys are scored against: under an FP8 cache the
+    decode's query cast to E4M3 ([TS] "One tree attention", FP8 paragraph)."""
+    if not q_fp8:
+        return qv
+    from .fp8 import decode_e4m3, encode_e4m3
+    return decode_e4m3(encode_e4m3(qv))
+
+
+def window_query(qv, q_fp8: bool):
+    """The query the window keys are scored against: the unquantized one,
+    under an FP8 cache too (the same paragraph: the window kernel takes the
+    unquantized query)."""
+    return qv
+
+
 def window_attention(q, k_cache, v_cache, page_table, prefix_len, mask, positions, W: int, Hkv: int,
                      theta: float, page_size: int = 64, scale: Optional[float] = None,
                      q_rotated: bool = False, rope_out: Optional[str] = "bf16", kv_fp8: bool = False,
@@ -174,13 +190,14 @@ def window_attention(q, k_cache, v_cache, page_table, prefix_len, mask, position
     ``kv_fp8``: the caches hold E4M3 bytes, read as the values they encode
     (oracle.fp8.decode_e4m3; [TS] "One tree attention", FP8 paragraph: the
     cache is unscaled and its K/V are widened after loading). ``q_fp8``: the
-    query (rotated and rounded as above) is cast to E4M3 before the scores
-    (oracle.fp8.encode_e4m3; the same paragraph: the decode over an FP8 cache
-    takes the query cast to FP8).
+    prefix keys are scored against the query (rotated and rounded as above)
+    cast to E4M3 (oracle.fp8.encode_e4m3), the window keys against the query
+    as it is (the same paragraph: the decode over the committed prefix takes
+    the query cast to FP8, the window kernel the unquantized query).
     """
     rnd = round_bf16 if rope_out == "bf16" else (lambda a: a)
-    if kv_fp8 or q_fp8:
-        from .fp8 import decode_e4m3, encode_e4m3
+    if kv_fp8:
+        from .fp8 import decode_e4m3
     load = decode_e4m3 if kv_fp8 else widen
     q = np.asarray(q)
     B = len(prefix_len)
@@ -206,17 +223,15 @@ def window_attention(q, k_cache, v_cache, page_table, prefix_len, mask, position
             qv = widen(q[b * R + r])
             if not q_rotated:
                 qv = rnd(rope.rotate(qv, int(positions[b][r]), theta))
-            if q_fp8:
-                qv = decode_e4m3(encode_e4m3(qv))
+            qp, qw = prefix_query(qv, q_fp8), window_query(qv, q_fp8)
             for kv in range(Hkv):
                 hs = slice(kv * g, (kv + 1) * g)
-                keys = np.concatenate([Kp[kv], Kw[kv]], axis=0)          # [P + |win|][d]
-                vals = np.concatenate([Vp[kv], Vw[kv]], axis=0)
-                if keys.shape[0] == 0:                                   # nothing visible (R22)
+                vals = np.concatenate([Vp[kv], Vw[kv]], axis=0)         # [P + |win|][d]
+                if vals.shape[0] == 0:                                   # nothing visible: 0 and -inf
                     out[b * R + r, hs] = 0.0
                     lse2[b * R + r, hs] = -np.inf
                     continue
-                s = (qv[hs] @ keys.T) * scale                            # [g][keys]
+                s = np.concatenate([qp[hs] @ Kp[kv].T, qw[hs] @ Kw[kv].T], axis=1) * scale  # [g][keys]
                 m = s.max(axis=1, keepdims=True)
                 e = np.exp(s - m)
                 Z = e.sum(axis=1)

@@ -318,3 +318,23 @@ def test_fp8_mutations_caught(monkeypatch):
         monkeypatch.setattr(F8, "encode_e4m3", bad)
         assert _fails(PF.test_encode_matches_torch_below_saturation) or _fails(PF.test_encode_ties_to_even_and_saturates)
         monkeypatch.setattr(F8, "encode_e4m3", _ORIG_ENCODE)
+
+
+def test_fp8_query_split_mutations_caught(monkeypatch):
+    """The E4M3 query cast applied to the window keys as well, or to no key,
+    fails the pin that separates the two parts."""
+    import oracle.attention as AT
+    from tests import test_oracle_window as PW2
+    real_prefix = AT.prefix_query
+
+    def window_cast(qv, q_fp8):                # the window keys also see the cast query
+        return F8.decode_e4m3(F8.encode_e4m3(qv)) if q_fp8 else qv
+
+    def no_cast(qv, q_fp8):                    # the prefix keys see the unquantized query
+        return qv
+
+    for name, bad in (("window_query", window_cast), ("prefix_query", no_cast)):
+        monkeypatch.setattr(AT, name, bad)
+        assert _fails(PW2.test_fp8_query_scores_the_prefix_only), name
+        monkeypatch.undo()
+    assert AT.prefix_query is real_prefix

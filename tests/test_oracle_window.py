@@ -213,3 +213,30 @@ def test_fp8_query_cast():
     bound = 2.0 ** -4 * np.abs(q[:, :, None, :] * k[None, :, 0, None, :].transpose(0, 2, 1, 3)).sum(-1).max() \
         / math.sqrt(d) / math.log(2)
     assert np.abs(l1 - l0).max() <= bound
+
+
+def test_fp8_query_scores_the_prefix_only():
+    """q_fp8 casts the query for the prefix keys alone: with no prefix (only
+    window keys visible) the cast changes nothing, and with no window key
+    visible the result is that of a query cast beforehand. A cast applied to
+    the window keys too, or to neither part, fails one of the two."""
+    from oracle import fp8 as F8
+    rng = np.random.default_rng(93)
+    B, R, W, Hq, Hkv, d, page = 1, 3, 4, 4, 2, 16, 4
+    k = rng.normal(0, 1, (32, Hkv, d))
+    v = rng.normal(0, 1, (32, Hkv, d))
+    table = np.array([[3, 5, 1, 6]], np.int32)
+    q = rng.normal(0, 1, (B * R, Hq, d))
+    # window keys only (P = 0): every row sees some window keys
+    args0 = (k, v, table, [0], [[1, 3, 0b1101]], [[0, 0, 0]], W, Hkv, THETA)
+    o1, l1 = A.window_attention(q, *args0, page_size=page, q_rotated=True, q_fp8=True)
+    o0, l0 = A.window_attention(q, *args0, page_size=page, q_rotated=True)
+    assert np.array_equal(o1, o0) and np.array_equal(l1, l0)
+    # prefix keys only (mask 0): the same as casting the query first
+    args1 = (k, v, table, [9], [[0, 0, 0]], [[0, 0, 0]], W, Hkv, THETA)
+    q8 = F8.decode_e4m3(F8.encode_e4m3(q))
+    o1, l1 = A.window_attention(q, *args1, page_size=page, q_rotated=True, q_fp8=True)
+    o0, l0 = A.window_attention(q8, *args1, page_size=page, q_rotated=True)
+    assert np.array_equal(o1, o0) and np.array_equal(l1, l0)
+    o2, l2 = A.window_attention(q, *args1, page_size=page, q_rotated=True)
+    assert not np.allclose(l2, l1)
