@@ -96,7 +96,8 @@ struct PrepArgs {
   int32_t *err;
   int64_t max_prefix, capacity;  // capacity: page-table rows x page size
   int rows, R, W, Hq, heads_per_thread;   // rows = B*R query rows; W window keys per request
-  int to_e4m3;  // FP8 cache: store the (rotated, bf16-rounded) queries as E4M3 bytes
+  int to_e4m3;  // FP8 cache: store the (rotated, bf16-rounded) queries as E4M3 bytes, and the
+                // bf16 ones in `out` (read back there by the merge pass for the window keys)
   dts::RopeFreqs freqs;
 };
 
@@ -175,6 +176,8 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
       }
       *reinterpret_cast<uint2 *>(q8 + off) = make_uint2(b1[0], b1[1]);
       *reinterpret_cast<uint2 *>(q8 + off + D / 2) = make_uint2(b2[0], b2[1]);
+      *reinterpret_cast<uint4 *>(a.out + off) = x1[hh];
+      *reinterpret_cast<uint4 *>(a.out + off + D / 2) = x2[hh];
       continue;
     }
     *reinterpret_cast<uint4 *>(a.q_rot + off) = x1[hh];
@@ -424,10 +427,13 @@ __device__ __forceinline__ uint64_t widen_fp8_v_rows(uint8_t *tile, int r0, int 
 
 // F8: the K and V caches hold unscaled E4M3 bytes ([TS] "One tree attention",
 // FP8 paragraph: no structural change; the prefix decode takes the query cast
-// to FP8; the window's FP8 K/V are widened after loading). S = Q K^T runs as
-// an FP8 MMA (kind::f8f6f4) on the E4M3 query (rotated, rounded to bf16, then
-// cast) and the K tile as loaded. Warps 2 and 3 widen each V tile to f16 in
-// shared memory (64 rows each), and O += P V runs in f16 with P in f16.
+// to FP8; the window kernel takes the unquantized query and widens the
+// window's FP8 K/V after loading). This pass then covers the prefix keys only
+// (the host passes W = 0) and leaves a partial for every unit; the merge pass
+// adds the window keys. S = Q K^T runs as an FP8 MMA (kind::f8f6f4) on the
+// E4M3 query (rotated, rounded to bf16, then cast) and the K tile as loaded.
+// Warps 2 and 3 widen each V tile to f16 in shared memory (64 rows each), and
+// O += P V runs in f16 with P in f16.
 template <int D, bool F8>
 __global__ void __launch_bounds__(384, 1)
     tree_prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -832,7 +838,9 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     while (ok && walker.next(a, sg)) {
       const uint32_t wpar = static_cast<uint32_t>(wcnt++) & 1u;  // win_bar completes once per segment
-      const bool whole = sg.lt0 == 0 && sg.lt1 == sg.nkt;        // the unit lies inside this segment
+      // the unit lies inside this segment (F8: the merge pass adds the window
+      // keys to every unit, so every unit leaves a partial)
+      const bool whole = !F8 && sg.lt0 == 0 && sg.lt1 == sg.nkt;
       if (t >= sg.nt) continue;
       const int nkt = sg.lt1 - sg.lt0;
       const int prow = t * a.rt + r;                      // row within the unit's slot
@@ -1044,8 +1052,17 @@ struct MergeArgs {
   uint16_t *out;
   float *lse2;
   int64_t max_prefix, capacity;
-  int B, R, W, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;
+  int B, R, W, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;  // W: window keys of the tree pass
   int owners32;  // every (tile index + 1) * groups fits in 32 bits
+  // F8 only: the window part, from the bf16 rotated queries the prep pass
+  // left in `out`, the mask and the E4M3 window K/V in the paged cache
+  const uint64_t *mask;
+  const uint8_t *k8, *v8;
+  const int32_t *page_table;
+  int32_t *err;
+  int64_t num_slots;
+  int Ww, max_pages, page_shift;  // Ww: window keys of the window part
+  float scale_log2;
 };
 
 // Which group's range holds flat tile x, and whether group c owns any tile:
@@ -1066,14 +1083,66 @@ struct Owners {
   }
 };
 
+// F8 window part of one row: the row's visible window keys (bits of `bits`)
+// scored against its bf16 rotated query q[] (this lane's E columns) with the
+// E4M3 K rows widened exactly, an online softmax in base 2 (m, l) and the
+// unnormalised sum of the widened V rows in o[]. A non-finite K or V row
+// turns the rows that see it NaN. Returns false (after reporting) when a
+// window slot lies outside the cache; the row then reads NaN.
+template <int D>
+__device__ bool window_part_f8(const MergeArgs &a, int b, int hkv, int P, uint64_t bits, const float (&q)[D / 32],
+                               int lane, float &m, float &l, float (&o)[D / 32]) {
+  constexpr int E = D / 32;
+  static_assert(E == 4, "the E4M3 cache takes d = 128");
+  m = -INFINITY;
+  l = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  const int ps = 1 << a.page_shift;
+  while (bits != 0ull) {
+    const int j = __ffsll(static_cast<long long>(bits)) - 1;
+    bits &= bits - 1ull;
+    const int pos = P + j;
+    const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
+    const int64_t slot = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
+    if (page < 0 || slot >= a.num_slots) {
+      if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
+      return false;
+    }
+    const int64_t off = (slot * a.Hkv + hkv) * D + E * lane;
+    const uint32_t kw = *reinterpret_cast<const uint32_t *>(a.k8 + off);
+    const uint32_t vw = *reinterpret_cast<const uint32_t *>(a.v8 + off);
+    const uint32_t k01 = dts::e4m3x2_to_f16x2(kw & 0xFFFFu), k23 = dts::e4m3x2_to_f16x2(kw >> 16);
+    const uint32_t v01 = dts::e4m3x2_to_f16x2(vw & 0xFFFFu), v23 = dts::e4m3x2_to_f16x2(vw >> 16);
+    const float k[4] = {dts::f16_lo(k01), dts::f16_hi(k01), dts::f16_lo(k23), dts::f16_hi(k23)};
+    const float v[4] = {dts::f16_lo(v01), dts::f16_hi(v01), dts::f16_lo(v23), dts::f16_hi(v23)};
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dot = fmaf(q[e], k[e], dot);
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+    const float sc = dot * a.scale_log2;
+    const float m_new = fmaxf(m, sc);  // (a NaN score leaves m; its weight below is NaN)
+    const float corr = m == -INFINITY ? 0.f : exp2f(m - m_new);
+    const float p = sc == -INFINITY ? 0.f : exp2f(sc - m_new);
+    l = l * corr + p;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = o[e] * corr + p * v[e];
+    m = m_new;
+  }
+  return true;
+}
+
 // One warp per 8 consecutive rows of a unit's slot (lane l holds columns
-// [E l, E l + E), E = d/32). A unit whose key tiles all fell to one CTA was
-// written by the tree pass; the others merge their parts' partial rows by
-// their LSEs: O = sum_k 2^(lse_k - m) O_k / sum_k 2^(lse_k - m),
-// lse = m + log2(sum_k 2^(lse_k - m)), m the largest lse_k.
+// [E l, E l + E), E = d/32). Without F8 a unit whose key tiles all fell to
+// one CTA was written by the tree pass; the others merge their parts'
+// partial rows by their LSEs: O = sum_k 2^(lse_k - m) O_k / sum_k 2^(lse_k -
+// m), lse = m + log2(sum_k 2^(lse_k - m)), m the largest lse_k. Under F8
+// every unit comes here, its parts cover the prefix only, and the window
+// part (window_part_f8) joins the sum as one more part.
 // Parts go four at a time: lane = part * 8 + row reads one LSE and decides
 // once whether its group owns tiles; the row loads of the four parts follow.
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__ MergeArgs a) {
   constexpr int kRows = 8;
   constexpr int E = D / 32;
@@ -1088,12 +1157,13 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   const int uir = static_cast<int>(unit - static_cast<uint32_t>(b) * per_req);
   const int hkv = uir / a.n_pairs, pair = uir - hkv * a.n_pairs;
   const int P = a.prefix_len[b];
-  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + a.W > a.capacity) return;  // NaN rows from prep
-  const int nkt = (P + a.W + 127) >> 7;
+  if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + (F8 ? a.Ww : a.W) > a.capacity)
+    return;  // NaN rows from prep
+  const int nkt = (P + a.W + 127) >> 7;  // key tiles of the unit in the tree pass (F8: prefix only)
   const Owners own{a.tiles_before[a.B], a.grid, a.owners32 != 0};
   const int64_t start = a.tiles_before[b] + static_cast<int64_t>(uir) * nkt;
-  const int64_t c_first = own.of(start), c_last = own.of(start + nkt - 1);
-  if (c_first == c_last) return;  // one part: the tree pass wrote these rows
+  const int64_t c_first = nkt > 0 ? own.of(start) : 0, c_last = nkt > 0 ? own.of(start + nkt - 1) : -1;
+  if (!F8 && c_first == c_last) return;  // one part: the tree pass wrote these rows
 
   const int i_row = lane & 7;
   const int prow_l = rb * kRows + i_row;
@@ -1112,7 +1182,6 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   }
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-
   // pass 2: weights, their sum and the weighted rows
   float acc[kRows][E];
 #pragma unroll
@@ -1171,21 +1240,48 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
 #pragma unroll
   for (int i = 0; i < kRows; ++i) {
     const int prow = rb * kRows + i;
-    const float den_i = __shfl_sync(0xffffffffu, den, i);
-    const float mx_i = __shfl_sync(0xffffffffu, mx, i);
+    float den_i = __shfl_sync(0xffffffffu, den, i);
+    float mx_i = __shfl_sync(0xffffffffu, mx, i);
     const int R = pair * 2 * a.rt + prow;  // row of the KV head
     if (prow >= a.slot_rows || R >= a.M) continue;
     const int node = R / a.g;
-    const int64_t out_row = (static_cast<int64_t>(b) * a.R + node) * a.Hq + hkv * a.g + (R - node * a.g);
+    const int64_t node_row = static_cast<int64_t>(b) * a.R + node;
+    const int64_t out_row = node_row * a.Hq + hkv * a.g + (R - node * a.g);
+    float num[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) num[e] = acc[i][e];
+    if constexpr (F8) {
+      // the window part: the prefix parts (lse mx_i, weight den_i) and the
+      // window keys (max m_w, weight l_w) meet at their common maximum
+      float q[E];
+      if constexpr (E == 4) {
+        const uint2 qw = *reinterpret_cast<const uint2 *>(a.out + out_row * D + E * lane);
+        q[0] = dts::bf16_lo(qw.x);
+        q[1] = dts::bf16_hi(qw.x);
+        q[2] = dts::bf16_lo(qw.y);
+        q[3] = dts::bf16_hi(qw.y);
+      }
+      const uint64_t bits = a.mask[node_row] & (a.Ww < 64 ? (1ull << a.Ww) - 1ull : ~0ull);
+      float m_w, l_w, o_w[E];
+      bool slot_ok = true;
+      if constexpr (E == 4) slot_ok = window_part_f8<D>(a, b, hkv, P, bits, q, lane, m_w, l_w, o_w);
+      const float M2 = fmaxf(mx_i, m_w);
+      const float ap = mx_i == -INFINITY ? 0.f : exp2f(mx_i - M2);
+      const float aw = m_w == -INFINITY ? 0.f : exp2f(m_w - M2);
+#pragma unroll
+      for (int e = 0; e < E; ++e) num[e] = ap * num[e] + aw * o_w[e];
+      den_i = ap * den_i + aw * l_w;
+      mx_i = M2;
+      if (!slot_ok) den_i = __int_as_float(0x7FC00000);
+    }
     const float inv = den_i == 0.f ? 0.f : 1.f / den_i;  // (a NaN sum stays NaN)
     if constexpr (E == 4) {
       uint2 v;
-      v.x = dts::pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
-      v.y = dts::pack_bf16x2(acc[i][2] * inv, acc[i][3] * inv);
+      v.x = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
+      v.y = dts::pack_bf16x2(num[2] * inv, num[3] * inv);
       *reinterpret_cast<uint2 *>(a.out + out_row * D + E * lane) = v;
     } else {
-      *reinterpret_cast<uint32_t *>(a.out + out_row * D + E * lane) =
-          dts::pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
+      *reinterpret_cast<uint32_t *>(a.out + out_row * D + E * lane) = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
     }
     if (lane == 0) a.lse2[out_row] = den_i == 0.f ? -INFINITY : mx_i + __log2f(den_i);
   }
@@ -1363,7 +1459,7 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   pa.max_prefix = max_prefix;
   pa.B = B;
   pa.R = R;
-  pa.W = W;
+  pa.W = f8 ? 0 : W;  // F8: the tree pass covers the prefix; the merge pass adds the window
   pa.Hq = Hq;
   pa.Hkv = Hkv;
   pa.g = g;
@@ -1392,7 +1488,17 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   ma.capacity = static_cast<int64_t>(max_pages) << page_shift;
   ma.B = B;
   ma.R = R;
-  ma.W = W;
+  ma.W = pa.W;
+  ma.Ww = W;
+  ma.mask = mask;
+  ma.k8 = static_cast<const uint8_t *>(k_cache);
+  ma.v8 = static_cast<const uint8_t *>(v_cache);
+  ma.page_table = page_table;
+  ma.err = err_dev;
+  ma.num_slots = num_slots;
+  ma.max_pages = max_pages;
+  ma.page_shift = page_shift;
+  ma.scale_log2 = scale * kLog2e;
   ma.Hq = Hq;
   ma.Hkv = Hkv;
   ma.g = g;
@@ -1403,13 +1509,14 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   ma.grid = grid;
   {
     // the largest possible tile total, times the groups, against 2^32
-    const int64_t max_tiles = static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + W + 127) / 128);
+    const int64_t max_tiles = static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + pa.W + 127) / 128);
     ma.owners32 = static_cast<double>(max_tiles + 1) * grid < 4294967296.0 ? 1 : 0;
   }
   const int64_t warps = plan.units * ((plan.slot_rows + 7) / 8);
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  if (d == 128) tree_merge_kernel<128><<<blocks, 256, 0, s>>>(ma);
-  else tree_merge_kernel<64><<<blocks, 256, 0, s>>>(ma);
+  if (f8) tree_merge_kernel<128, true><<<blocks, 256, 0, s>>>(ma);
+  else if (d == 128) tree_merge_kernel<128, false><<<blocks, 256, 0, s>>>(ma);
+  else tree_merge_kernel<64, false><<<blocks, 256, 0, s>>>(ma);
   return dts_host::launch_status();
 }
 
