@@ -28,7 +28,7 @@ EXPORTED = (
     "dts_tree_verify_attention_static_ws", "dts_target_argmax_workspace", "dts_target_argmax",
     "dts_verify_tree_greedy_logits", "dts_tree_window_attention_workspace", "dts_tree_window_attention",
     "dts_sample_draws", "dts_verify_tree_sampled", "dts_write_window_kv_fp8", "dts_tree_window_attention_fp8",
-    "dts_tree_verify_attention_fp8",
+    "dts_tree_verify_attention_fp8", "dts_test_stall_attention",
 )
 
 
@@ -74,6 +74,7 @@ _SIGS = {
     "dts_verify_tree_greedy_logits": (_I, [_P, _P, _I, _L, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "dts_compact_window_rows": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P]),
     "dts_compact_rows": (_I, [_P, _L, _P, _P, _P, _P, _I, _I, _P, _P]),
+    "dts_test_stall_attention": (_I, [_I, ctypes.c_longlong]),
 }
 
 

@@ -42,6 +42,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -201,6 +202,8 @@ struct PrefixArgs {
   int64_t num_slots, max_prefix;
   int B, R, W, Hq, Hkv, g, M, rt, npt, n_pairs, slot_rows, max_pages, page_shift;  // R rows, W window keys per request
   float scale_log2;
+  long long wait_budget;  // cycles before a bounded wait gives up
+  int stall;              // test hook: the producer issues no copy at all
 };
 
 template <int D>
@@ -293,6 +296,11 @@ __device__ __forceinline__ uint32_t visible_word(int o, uint64_t mrow) {
 constexpr uint32_t kP0Threads = 128 + 32 + 32;
 constexpr uint32_t kP1Threads = 128 + 32;
 __device__ __forceinline__ uint32_t p_bar_threads(int t) { return t == 0 ? kP0Threads : kP1Threads; }
+// Named-barrier operations are warp-aligned: the branches leading to them
+// must be the same in every lane, so the result of a bounded wait that
+// decides such a branch is taken for the whole warp.
+__device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
+
 __device__ __forceinline__ uint32_t p_bar_id(int t, int r) {
   return 1u + 2u * static_cast<uint32_t>(t) + (static_cast<uint32_t>(r) & 1u);
 }
@@ -522,6 +530,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const long long wait_budget = a.wait_budget;
   const int64_t total = range[0];
   const int64_t x0 = total * blockIdx.x / gridDim.x;
   const int64_t x1 = total * (blockIdx.x + 1) / gridDim.x;
@@ -550,7 +559,9 @@ __global__ void __launch_bounds__(384, 1)
       constexpr int kRowBoxes = F8 ? 1 : D / 64;
       int use = 0, segc = 0;
       bool ok = true;
-      while (ok && walker.next(a, sg)) {
+      // (a.stall, a test hook: no copy is ever issued, so the consumers' waits
+      // run out and the kernel leaves with DTS_DEV_TIMEOUT)
+      while (ok && a.stall == 0 && walker.next(a, sg)) {
         const int64_t pt_row = static_cast<int64_t>(sg.b) * a.max_pages;
         int batch_base = -(1 << 30);
         int my_pid = -1;
@@ -572,7 +583,7 @@ __global__ void __launch_bounds__(384, 1)
           return static_cast<int>(s0);
         };
         // the unit's query tiles
-        if (!mbar_wait(q_empty, (static_cast<uint32_t>(segc) & 1u) ^ 1u, abort_flag)) {
+        if (!mbar_wait(q_empty, (static_cast<uint32_t>(segc) & 1u) ^ 1u, abort_flag, wait_budget)) {
           ok = false;
           break;
         }
@@ -594,7 +605,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int kv = 0; kv < 2; ++kv, ++use) {
             const int slot = use % kSlots;
             const uint32_t ph = static_cast<uint32_t>(use / kSlots) & 1u;
-            if (!mbar_wait(&empty[slot], ph ^ 1u, abort_flag)) {
+            if (!mbar_wait(&empty[slot], ph ^ 1u, abort_flag, wait_budget)) {
               ok = false;
               break;
             }
@@ -616,9 +627,11 @@ __global__ void __launch_bounds__(384, 1)
       if (!ok) {
         if (lane == 0) {
           dts::report(a.err, DTS_DEV_TIMEOUT);
-          // give the copies already in flight a bounded chance to land
+          // the copies already in flight land before the CTA's shared memory
+          // goes (bounded, whatever the abort flag says)
           for (int u = max(0, use - kSlots); u < use; ++u)
-            mbar_wait((u & 1) ? &vfull[u % kSlots] : &kfull[u % kSlots], kind_phase<kSlots>(u), abort_flag);
+            mbar_wait_own((u & 1) ? &vfull[u % kSlots] : &kfull[u % kSlots], kind_phase<kSlots>(u), wait_budget);
+          if (segc > 0) mbar_wait_own(q_full, static_cast<uint32_t>(segc - 1) & 1u, wait_budget);
         }
       }
       __syncwarp();
@@ -668,8 +681,8 @@ __global__ void __launch_bounds__(384, 1)
         const int nkt = sg.lt1 - sg.lt0;
         const int nt = sg.nt;
         // S for the segment's first tile needs its Q tiles and K
-        ok = mbar_wait(q_full, static_cast<uint32_t>(segc) & 1u, abort_flag) &&
-             mbar_wait(&kfull[slot_of(use)], kind_phase_of(use), abort_flag);
+        ok = warp_all(mbar_wait(q_full, static_cast<uint32_t>(segc) & 1u, abort_flag, wait_budget) &&
+                      mbar_wait(&kfull[slot_of(use)], kind_phase_of(use), abort_flag, wait_budget));
         if (!ok) break;
         tc_fence_after();
         int kslot = slot_of(use);  // the slot of K(j + 1) in the loop below, of K(0) here
@@ -748,7 +761,7 @@ __global__ void __launch_bounds__(384, 1)
       // drain: wait for every MMA issued so far before TMEM is released
       if (lane == 0) mma_commit(drain);
       __syncwarp();
-      mbar_wait(drain, 0, abort_flag);
+      mbar_wait_own(drain, 0, wait_budget);
     } else {
       // ---------------------------------------------------------- V-tile warp(s), voucher
       // Warp 2 (and warp 3 under F8) hands every V tile on (vready) once it
@@ -772,7 +785,7 @@ __global__ void __launch_bounds__(384, 1)
           const int vuse = use + 2 * j + 1;
           const int vslot = vuse % kSlots;
           if (v_role) {
-            ok = mbar_wait(&vfull[vslot], kind_phase<kSlots>(vuse), abort_flag);
+            ok = warp_all(mbar_wait(&vfull[vslot], kind_phase<kSlots>(vuse), abort_flag, wait_budget));
             if (!ok) break;
             const int kbase = (sg.lt0 + j) * 128;
             if constexpr (F8) {
@@ -786,8 +799,9 @@ __global__ void __launch_bounds__(384, 1)
           }
           if (voucher) {
             const int kuse = vuse + 1;
-            ok = mbar_wait(&vready[vslot], kind_phase<kSlots>(vuse), abort_flag) &&
-                 (j + 1 == nkt || mbar_wait(&kfull[kuse % kSlots], kind_phase<kSlots>(kuse), abort_flag));
+            ok = warp_all(mbar_wait(&vready[vslot], kind_phase<kSlots>(vuse), abort_flag, wait_budget) &&
+                          (j + 1 == nkt ||
+                           mbar_wait(&kfull[kuse % kSlots], kind_phase<kSlots>(kuse), abort_flag, wait_budget)));
             if (!ok) break;
             named_sync(p_bar_id(0, rounds), kP0Threads);
             ++rounds;
@@ -803,7 +817,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t)
             if (ok && t < prev_nt && scnt[t] > 0)
-              ok = mbar_wait(&o_free[t], static_cast<uint32_t>(scnt[t] - 1) & 1u, abort_flag);
+              ok = warp_all(mbar_wait(&o_free[t], static_cast<uint32_t>(scnt[t] - 1) & 1u, abort_flag, wait_budget));
           prev_nt = sg.nt;
 #pragma unroll
           for (int t = 0; t < 2; ++t)
@@ -856,7 +870,7 @@ __global__ void __launch_bounds__(384, 1)
         const bool in_window = (sg.lt0 + j) * 128 + 128 > sg.P;
         uint64_t mrow = 0;
         if (in_window) mrow = row_mask();  // in flight during the wait below
-        if (!mbar_wait(&s_full[t], static_cast<uint32_t>(tcnt + j) & 1u, abort_flag)) {
+        if (!warp_all(mbar_wait(&s_full[t], static_cast<uint32_t>(tcnt + j) & 1u, abort_flag, wait_budget))) {
           ok = false;
           break;
         }
@@ -950,8 +964,8 @@ __global__ void __launch_bounds__(384, 1)
         named_arrive(p_bar_id(t, arrived), p_bar_threads(t));
         ++arrived;
       }
-      if (!ok || !mbar_wait(&o_fin[t], static_cast<uint32_t>(scnt) & 1u, abort_flag) ||
-          !mbar_wait(win_bar, wpar, abort_flag)) {
+      if (!ok || !warp_all(mbar_wait(&o_fin[t], static_cast<uint32_t>(scnt) & 1u, abort_flag, wait_budget) &&
+                           mbar_wait(win_bar, wpar, abort_flag, wait_budget))) {
         ok = false;
         break;
       }
@@ -1290,6 +1304,11 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
 // ============================================================================
 // host side
 // ============================================================================
+// Test hook (dts_test_stall_attention): the wait budget of the tree pass and
+// whether its producer issues nothing.
+std::atomic<long long> g_test_wait_budget{dts::ptx::kWaitBudget};
+std::atomic<int> g_test_stall{0};
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1471,6 +1490,8 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   pa.max_pages = max_pages;
   pa.page_shift = page_shift;
   pa.scale_log2 = scale * kLog2e;
+  pa.wait_budget = g_test_wait_budget.load(std::memory_order_relaxed);
+  pa.stall = g_test_stall.load(std::memory_order_relaxed);
   const int st = f8          ? launch_prefix<128, true>(tk, tv, tq, pa, grid, s)
                  : d == 128 ? launch_prefix<128, false>(tk, tv, tq, pa, grid, s)
                             : launch_prefix<64, false>(tk, tv, tq, pa, grid, s);
@@ -1675,4 +1696,13 @@ extern "C" int dts_tree_verify_attention_static_ws(const uint16_t *q, const uint
   return dts_tree_verify_attention(q, k_cache, v_cache, num_slots, page_table, max_pages, page_size, prefix_len,
                                    max_prefix, mask, positions, rope_theta, B, N, Hq, Hkv, d, softmax_scale, out,
                                    lse2, ws, kStaticWorkspaceBytes, err_dev, stream);
+}
+
+// Test hook: see include/dts.h.
+extern "C" int dts_test_stall_attention(int stall, long long wait_budget_cycles) {
+  if (stall != 0 && stall != 1) return DTS_ERR_INVALID;
+  if (wait_budget_cycles < (1ll << 16) || wait_budget_cycles > dts::ptx::kWaitBudget) return DTS_ERR_INVALID;
+  g_test_stall.store(stall, std::memory_order_relaxed);
+  g_test_wait_budget.store(stall ? wait_budget_cycles : dts::ptx::kWaitBudget, std::memory_order_relaxed);
+  return DTS_OK;
 }

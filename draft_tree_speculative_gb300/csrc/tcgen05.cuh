@@ -47,20 +47,35 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 // ~2^31 cycles (about a second at GB300 clocks) before a wait gives up.
 constexpr long long kWaitBudget = 1ll << 31;
 
-// Wait for the phase of `parity` to complete. Returns false if the budget ran
-// out or another role of the CTA already gave up (abort flag set).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+// Wait for the phase of `parity` to complete. Returns false if `budget`
+// cycles ran out (and then sets the abort flag) or another role of the CTA
+// already gave up (abort flag set).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          long long budget = kWaitBudget) {
   if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitBudget) {
+      if (clock64() - t0 > budget) {
         *abort_flag = 1;
         return false;
       }
     }
+  }
+}
+
+// The same wait without the abort flag: a role that is leaving waits here for
+// its own asynchronous work (copies it issued, MMAs it issued) to finish, so
+// that shared and tensor memory are released only once nothing writes them.
+// Bounded by `budget` all the same; returns false if it ran out.
+__device__ __forceinline__ bool mbar_wait_own(uint64_t *bar, uint32_t parity, long long budget = kWaitBudget) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 255u) == 0 && clock64() - t0 > budget) return false;
   }
 }
 

@@ -507,6 +507,25 @@ int dts_compact_rows(void *hidden, int64_t row_bytes, int32_t *positions, const 
                      const int32_t *accepted_path, const int32_t *accept_len, int B, int N,
                      int32_t *err_dev, dts_stream_t stream);
 
+/*
+ * dts_test_stall_attention - test hook, not a step of the verify path (the
+ * pages have no counterpart). It lets a test make the tensor-core tree pass
+ * give up on purpose, without a fault: with stall = 1, the pass's producer
+ * issues no copy at all in the attention calls launched afterwards (every
+ * tree/window attention entry point, bf16 and E4M3), so the waits of the other
+ * roles run out after wait_budget_cycles; the kernel then frees its tensor
+ * memory, returns, and *err_dev reads DTS_DEV_TIMEOUT. The outputs of such a
+ * call are undefined. stall = 0 restores normal operation (the budget goes
+ * back to about 2^31 cycles). The setting is process-wide; calls that overlap
+ * with a change of it see either setting.
+ *
+ *   stall               0 or 1
+ *   wait_budget_cycles  2^16 .. 2^31 (used only with stall = 1)
+ *
+ * Returns DTS_OK, or DTS_ERR_INVALID for values outside those ranges.
+ */
+int dts_test_stall_attention(int stall, long long wait_budget_cycles);
+
 #ifdef __cplusplus
 }
 #endif

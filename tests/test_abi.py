@@ -139,3 +139,13 @@ def test_static_workspace_validates_like_the_regular_call(lib):
     big = dict(B=32, N=64, ptr=4096)
     assert dts.tree_verify_attention_workspace(32, 64, 32, 8, 128, 0) > (64 << 20)
     assert both(**big) == (dts.ERR_WORKSPACE, dts.ERR_WORKSPACE)
+
+
+def test_stall_hook_validates(lib):
+    """The test hook takes stall 0 or 1 and a budget of 2^16 .. 2^31 cycles;
+    anything else is refused, and stall = 0 leaves normal operation."""
+    L = dts.lib()
+    assert L.dts_test_stall_attention(2, 1 << 20) == dts.ERR_INVALID
+    assert L.dts_test_stall_attention(1, 100) == dts.ERR_INVALID
+    assert L.dts_test_stall_attention(1, 1 << 40) == dts.ERR_INVALID
+    assert L.dts_test_stall_attention(0, 1 << 31) == dts.OK

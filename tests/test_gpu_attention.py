@@ -12,8 +12,8 @@ from draft_tree_speculative_gb300 import synth
 from draft_tree_speculative_gb300.step import DeviceBatch, run_step
 from oracle import attention as OA
 from oracle import rope as OR
-from tests.gpu_helpers import (assert_attention_close, bf16_bits_of, bf16_to_f64, custom_workload, random_tree,
-                               torch_cuda)
+from tests.gpu_helpers import (assert_attention_close, bf16_bits_of, bf16_to_f64, custom_workload, oracle_every_row,
+                               random_tree, torch_cuda)
 
 pytestmark = pytest.mark.gpu
 
@@ -88,25 +88,15 @@ def test_attention_small_workloads_all_rows(name):
     assert_attention_close(out, lse, ref_o, ref_l, range(inp.w.B * inp.w.N))
 
 
-def _sample_rows(w, parents, rng, k):
-    rows = {(0, 0), (w.B - 1, w.N - 1)}
-    deep = int(np.argmax(synth.depth_of(parents[0])))
-    rows.add((0, deep))
-    while len(rows) < k:
-        rows.add((int(rng.integers(0, w.B)), int(rng.integers(0, w.N))))
-    return sorted(rows)
-
-
-@pytest.mark.parametrize("name,k", [("eagle2_p8192_n64", 24), ("longctx_p131072_n64", 8), ("highconc_b128_n16", 24)])
-def test_attention_full_size_sampled_rows(name, k):
+@pytest.mark.parametrize("name", ["eagle2_p8192_n64", "longctx_p131072_n64", "highconc_b128_n16"])
+def test_attention_full_size_every_row(name):
     """Full-size workload in the launch configuration the benchmark times;
-    the oracle recomputes a sample of rows (all heads) one by one."""
+    the oracle recomputes every row (all heads), spread over host processes."""
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w)
     _, out, lse = _run_attention(inp)
-    rows = _sample_rows(w, inp.parents, np.random.default_rng(7), k)
-    ref_o, ref_l = _oracle(inp, rows=rows)
-    assert_attention_close(out, lse, ref_o, ref_l, [b * w.N + v for b, v in rows])
+    ref_o, ref_l = oracle_every_row("bf16", name)
+    assert_attention_close(out, lse, ref_o, ref_l, range(w.B * w.N))
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 

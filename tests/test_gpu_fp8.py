@@ -21,7 +21,8 @@ from draft_tree_speculative_gb300 import synth
 from oracle import attention as OA
 from oracle import fp8 as F8
 from oracle import tree as OT
-from tests.gpu_helpers import assert_attention_close, bf16_to_f64, custom_workload, random_tree, torch_cuda
+from tests.gpu_helpers import (assert_attention_close, bf16_to_f64, custom_workload, oracle_every_row, random_tree,
+                               torch_cuda)
 
 pytestmark = pytest.mark.gpu
 
@@ -103,12 +104,15 @@ def test_verify_fp8_llama8b_all_rows():
     _check_verify(inp, k8, v8, range(inp.w.B), out, lse)
 
 
-def test_verify_fp8_eagle2_full_size_sampled_requests():
+def test_verify_fp8_eagle2_full_size_every_row():
     """The EAGLE-2 batch at full size (32 requests x 64 nodes, P = 8192) in
-    the launch the bench times; three requests' rows compared in full."""
-    inp, k8, v8 = _verify_case(synth.WORKLOADS["eagle2_p8192_n64"])
+    the launch the bench times; every row compared (the oracle spread over
+    host processes)."""
+    w = synth.WORKLOADS["eagle2_p8192_n64"]
+    inp, k8, v8 = _verify_case(w)
     out, lse = _run_verify_fp8(inp, k8, v8, rotate=False)
-    _check_verify(inp, k8, v8, [0, 13, 31], out, lse, rotate=False)
+    ro, rl = oracle_every_row("fp8", w.name, rotate=False)
+    assert_attention_close(out, lse, ro, rl, range(w.B * w.N))
 
 
 @pytest.mark.parametrize("i, over, kind", [
