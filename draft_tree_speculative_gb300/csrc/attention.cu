@@ -234,37 +234,50 @@ struct Segment {
   int64_t start;  // flat index of the unit's first key tile
 };
 
-// Walks the flat key-tile range [x, x1) as segments, in order.
+// Walks the flat key-tile range [x, x1) as segments, in order. The flat
+// order is (row pair, request, KV head, key tile): all units of the first
+// 256 rows of every KV head, then those of the next 256 rows in the same
+// order. With two pairs (M = 512) the two halves of the range mirror each
+// other, so CTA c and CTA c + G/2 read the same K/V tiles at about the same
+// time and the second read comes from L2.
 struct SegmentWalker {
   int b;
   int nkt;
-  int64_t tb;  // tiles of all units of requests < b
+  int64_t tb;     // tiles of the units of requests < b within the current pair
+  int64_t pbase;  // flat index of the current pair's first tile
+  int64_t half;   // tiles of one pair (every request, every KV head)
   int64_t x, x1;
 
-  __device__ void init(const PrefixArgs &a, int64_t x0, int64_t x_end) {
+  __device__ void init(const PrefixArgs &a, int64_t x0, int64_t x_end, int64_t pair_tiles) {
     b = 0;
     tb = 0;
+    half = pair_tiles;
+    pbase = half > 0 ? x0 / half * half : 0;
     nkt = a.B > 0 ? request_tiles(a.prefix_len, 0, a.max_prefix, a.W, a.max_pages, a.page_shift) : 0;
     x = x0;
     x1 = x_end;
   }
   __device__ bool next(const PrefixArgs &a, Segment &s) {
     if (x >= x1) return false;
-    const int64_t per_req = static_cast<int64_t>(a.Hkv) * a.n_pairs;
-    while (x >= tb + nkt * per_req) {
-      tb += nkt * per_req;
-      ++b;
+    while (x >= pbase + tb + static_cast<int64_t>(nkt) * a.Hkv) {
+      tb += static_cast<int64_t>(nkt) * a.Hkv;
+      if (++b == a.B) {  // the next pair's units
+        b = 0;
+        tb = 0;
+        pbase += half;
+      }
       nkt = request_tiles(a.prefix_len, b, a.max_prefix, a.W, a.max_pages, a.page_shift);
     }
-    const int64_t off = x - tb;
-    const int uir = static_cast<int>(off / nkt);
+    const int64_t off = x - pbase - tb;
     s.b = b;
-    s.hkv = uir / a.n_pairs;
-    s.pair = uir - s.hkv * a.n_pairs;
-    s.unit = static_cast<int>(static_cast<int64_t>(b) * per_req + uir);
+    s.hkv = static_cast<int>(off / nkt);
+    s.pair = static_cast<int>(pbase / half);
+    // units numbered in the flat order, so that a partial's slot (unit + CTA
+    // index) grows with the flat index and no two segments share one
+    s.unit = (s.pair * a.B + b) * a.Hkv + s.hkv;
     s.nkt = nkt;
-    s.start = tb + static_cast<int64_t>(uir) * nkt;
-    s.lt0 = static_cast<int>(off - static_cast<int64_t>(uir) * nkt);
+    s.start = pbase + tb + static_cast<int64_t>(s.hkv) * nkt;
+    s.lt0 = static_cast<int>(off - static_cast<int64_t>(s.hkv) * nkt);
     s.lt1 = static_cast<int>(min(static_cast<int64_t>(nkt), s.lt0 + (x1 - x)));
     s.P = a.prefix_len[b];
     const int rows_left = a.M - s.pair * 2 * a.rt;
@@ -505,7 +518,7 @@ __global__ void __launch_bounds__(384, 1)
       part += static_cast<int64_t>(request_tiles(a.prefix_len, b, a.max_prefix, a.W, a.max_pages, a.page_shift));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) range[0] = part * a.Hkv * a.n_pairs;
+    if (lane == 0) range[0] = part * a.Hkv * a.n_pairs;  // n_pairs mirror-image halves
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
@@ -517,12 +530,13 @@ __global__ void __launch_bounds__(384, 1)
     tmem_relinquish();
   }
   if (warp == 3 && blockIdx.x == 0 && lane == 0) {
-    // tiles-before table for the merge pass
+    // tiles-before table for the merge pass (within one row pair; the last
+    // entry is the tiles of one pair)
     int64_t acc = 0;
     for (int b = 0; b < a.B; ++b) {
       a.tiles_before[b] = acc;
       acc += static_cast<int64_t>(request_tiles(a.prefix_len, b, a.max_prefix, a.W, a.max_pages, a.page_shift)) *
-             a.Hkv * a.n_pairs;
+             a.Hkv;
     }
     a.tiles_before[a.B] = acc;
   }
@@ -537,7 +551,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sQ_addr = smem_addr(sQ);
   const uint32_t sKV_addr = smem_addr(sKV);
   SegmentWalker walker;
-  walker.init(a, x0, x1);
+  walker.init(a, x0, x1, total / a.n_pairs);
   Segment sg;
 
   // Register split: the control warpgroup (TMA, MMA) gives registers to the
@@ -1012,21 +1026,48 @@ __global__ void __launch_bounds__(384, 1)
         // combines the unit's partials)
         const int64_t slot_row = (static_cast<int64_t>(sg.unit) + blockIdx.x) * a.slot_rows + prow;
         if (warp_valid) {
-          float *dst = a.o_part + slot_row * D;
+          // Thread = row, and a row of the partial is 4 D contiguous bytes:
+          // stored straight, every 16-byte store would hit another row, and
+          // the epilogue runs at the rate of partial-sector writes. So each
+          // 8-lane group transposes its 8 rows x 8 float4 units of a 32-column
+          // chunk (three xor-butterfly stages) and then writes one row's 128
+          // contiguous bytes per store.
+          const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+          const int grp = lane & ~7, cu = lane & 7;
+          float *dst0 = a.o_part + (slot_row - cu) * D + 4 * cu;  // row grp + 0, this lane's unit
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
             uint32_t ov[32];
             tmem_ld32(tO + q * 32, ov);
             tmem_wait_ld();
-            if (valid) {
+            float4 u[8];
 #pragma unroll
-              for (int k = 0; k < 32; k += 4) {
-                float4 v = make_float4(__uint_as_float(ov[k]) * inv_l, __uint_as_float(ov[k + 1]) * inv_l,
-                                       __uint_as_float(ov[k + 2]) * inv_l, __uint_as_float(ov[k + 3]) * inv_l);
-                if (poisoned) v = make_float4(NAN, NAN, NAN, NAN);
-                *reinterpret_cast<float4 *>(dst + q * 32 + k) = v;
+            for (int k = 0; k < 8; ++k) {
+              u[k] = make_float4(__uint_as_float(ov[4 * k]) * inv_l, __uint_as_float(ov[4 * k + 1]) * inv_l,
+                                 __uint_as_float(ov[4 * k + 2]) * inv_l, __uint_as_float(ov[4 * k + 3]) * inv_l);
+              if (poisoned) u[k] = make_float4(NAN, NAN, NAN, NAN);
+            }
+#pragma unroll
+            for (int mi = 0; mi < 3; ++mi) {
+              const int m = 4 >> mi;
+              const bool hi = (lane & m) != 0;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (k & m) continue;
+                const float4 snd = hi ? u[k] : u[k | m];
+                float4 rcv;
+                rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
+                rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
+                rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
+                rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
+                if (hi) u[k] = rcv;
+                else u[k | m] = rcv;
               }
             }
+            // this lane now holds unit cu of rows grp .. grp + 7
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+              if ((vmask >> (grp + r)) & 1u) *reinterpret_cast<float4 *>(dst0 + r * D + q * 32) = u[r];
           }
           if (valid) a.lse_part[slot_row] = lse_row;
         }
@@ -1164,18 +1205,19 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   const uint32_t wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t blocks_per_unit = static_cast<uint32_t>((a.slot_rows + kRows - 1) / kRows);
   const uint32_t unit = wid / blocks_per_unit;
-  const uint32_t per_req = static_cast<uint32_t>(a.Hkv * a.n_pairs);
-  if (unit >= static_cast<uint32_t>(a.B) * per_req) return;
+  // units in the flat order of the tree pass: (row pair, request, KV head)
+  const uint32_t per_pair = static_cast<uint32_t>(a.B * a.Hkv);
+  if (unit >= per_pair * static_cast<uint32_t>(a.n_pairs)) return;
   const int rb = static_cast<int>(wid - unit * blocks_per_unit);
-  const int b = static_cast<int>(unit / per_req);
-  const int uir = static_cast<int>(unit - static_cast<uint32_t>(b) * per_req);
-  const int hkv = uir / a.n_pairs, pair = uir - hkv * a.n_pairs;
+  const int pair = static_cast<int>(unit / per_pair);
+  const int bh = static_cast<int>(unit - static_cast<uint32_t>(pair) * per_pair);
+  const int b = bh / a.Hkv, hkv = bh - b * a.Hkv;
   const int P = a.prefix_len[b];
   if (P < 0 || P > a.max_prefix || static_cast<int64_t>(P) + (F8 ? a.Ww : a.W) > a.capacity)
     return;  // NaN rows from prep
   const int nkt = (P + a.W + 127) >> 7;  // key tiles of the unit in the tree pass (F8: prefix only)
-  const Owners own{a.tiles_before[a.B], a.grid, a.owners32 != 0};
-  const int64_t start = a.tiles_before[b] + static_cast<int64_t>(uir) * nkt;
+  const Owners own{a.tiles_before[a.B] * a.n_pairs, a.grid, a.owners32 != 0};
+  const int64_t start = pair * a.tiles_before[a.B] + a.tiles_before[b] + static_cast<int64_t>(hkv) * nkt;
   const int64_t c_first = nkt > 0 ? own.of(start) : 0, c_last = nkt > 0 ? own.of(start + nkt - 1) : -1;
   if (!F8 && c_first == c_last) return;  // one part: the tree pass wrote these rows
 
