@@ -156,6 +156,19 @@ def recorded_instructions(name, workload):
     return e.get("warp_instructions_per_call")
 
 
+def run_ahead(stream, us=3000.0):
+    """Enqueue a GPU spin of about `us` microseconds on `stream`, outside any
+    timed events, so that the host enqueues the next steps while it runs and
+    the GPU then executes them back to back: device times then measure the
+    kernels, not the host's launch latency between small kernels."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2000))  # cycles, at about 2 GHz
+
+
+AHEAD_STEPS = 8  # timed steps enqueued behind each spin
+
+
 def check_device_error(db, when):
     from draft_tree_speculative_gb300 import device_error_string
     code = int(db.err.item())
@@ -321,10 +334,11 @@ def run_ours(args, rank, world, local_rank):
     db = DeviceBatch(inp, device=dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    names = ("mask", "window_kv", "attention", "walk", "compact")
-    calls = (db.mask_step, db.window_kv_step, db.attention_step, db.walk_step, db.compact_step)
-    # mask, window kv, attention (prep, tree pass, merge), walk, kv compaction, row compaction
-    launches_per_step = 8
+    # prologue (mask + window K/V), attention (prep, tree pass, merge),
+    # epilogue (walk + KV and hidden-row compaction): five launches
+    names = ("prologue", "attention", "epilogue")
+    calls = (db.prologue_step, db.attention_step, db.epilogue_step)
+    launches_per_step = DeviceBatch.KERNELS_PER_STEP
 
     def one_step(ev=None):
         for k, c in enumerate(calls):
@@ -349,6 +363,8 @@ def run_ours(args, rank, world, local_rank):
         wall0 = time.perf_counter()
         with torch.cuda.stream(stream):
             for s in range(args.steps):
+                if s % AHEAD_STEPS == 0:
+                    run_ahead(stream)
                 flush.fill_(1)
                 one_step(events[s])
         torch.cuda.synchronize()
@@ -435,9 +451,11 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the workload)",
         "config": {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
                    "prefix_len": int(inp.vc.max()), "page_size": w.page_size, "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every timed step (512 MiB write, outside the step's events)"},
+                   "l2": "flushed before every timed step (512 MiB write, outside the step's events)",
+                   "host": f"runs ahead of the device: a GPU spin outside the events before every {AHEAD_STEPS} "
+                           "steps lets the host enqueue them, so the device times are the kernels' own"},
         "roofline": roof,
-        "verify_tree_us": statistics.median(per_call["walk"]) * 1e3,
+        "verify_tree_us": time_walk(db, stream, args),
         "kernels_us": {n: statistics.median(v) * 1e3 for n, v in per_call.items()},
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_region": wall,
@@ -479,23 +497,23 @@ def time_side_workload(name, args, dev, stream, flush):
     then the compaction of every K/V buffer (the attention layer's bf16 K and V
     plus 2 x fp8_layers fp8 buffers) and of the hidden rows."""
     import torch
-    from draft_tree_speculative_gb300 import target_argmax_workspace, verify_tree_greedy_logits
+    from draft_tree_speculative_gb300 import target_argmax, target_argmax_workspace
     from draft_tree_speculative_gb300.step import DeviceBatch
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w)
     db = DeviceBatch(inp, device=dev)
     full = w.fp8_layers > 0
-    names = ["mask", "window_kv", "attention", "walk", "compact"]
-    calls = [db.mask_step, db.window_kv_step, db.attention_step, db.walk_step, db.compact_step]
+    names = ["prologue", "attention", "epilogue"]
+    calls = [db.prologue_step, db.attention_step, db.epilogue_step]
     logits = ws = arg = None
     if full:
         logits = torch.from_numpy(synth.target_logits(w, inp.target_argmax)).to(dev)
         arg = torch.empty((w.B, w.N), dtype=torch.int32, device=dev)
         ws = torch.empty(max(8, target_argmax_workspace(w.B * w.N, w.vocab)), dtype=torch.uint8, device=dev)
-        names[3] = "argmax_walk"
-        calls[3] = lambda st: verify_tree_greedy_logits(db.draft, logits, arg, db.accept_len, db.accepted_path,
-                                                         db.accepted_tokens, ws, parents=db.parents, err=db.err,
-                                                         stream=st)
+        names = ["prologue", "attention", "target_argmax", "epilogue"]
+        calls = [db.prologue_step, db.attention_step,
+                 lambda st: target_argmax(logits, arg.view(-1), ws, stream=st),
+                 lambda st: db.epilogue_step(st, target_argmax=arg)]
     reps = max(5, min(args.steps, 30))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
     with torch.cuda.stream(stream):
@@ -506,7 +524,9 @@ def time_side_workload(name, args, dev, stream, flush):
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         with torch.cuda.stream(stream):
-            for e in ev:
+            for r, e in enumerate(ev):
+                if r % AHEAD_STEPS == 0:
+                    run_ahead(stream)
                 flush.fill_(1)
                 for k, c in enumerate(calls):
                     e[k].record(stream)
@@ -527,16 +547,36 @@ def time_side_workload(name, args, dev, stream, flush):
         out["clocks"] = clocks
     if full:
         out["full_step_us"] = step_us
-        out["full_step"] = ("mask, window K/V, attention, target argmax over fp32 logits "
-                            f"[{w.B * w.N}][{w.vocab}] + walk, compaction of {len(db.kv_entries)} K/V buffers "
-                            f"({2 * w.fp8_layers} fp8 layers' K and V plus the bf16 attention layer) and hidden rows "
-                            f"[{w.B * w.N}][{inp.hidden.shape[1]}]")
+        out["full_step"] = ("prologue (mask + window K/V), attention, target argmax over fp32 logits "
+                            f"[{w.B * w.N}][{w.vocab}], epilogue (walk + compaction of {len(db.kv_entries)} K/V "
+                            f"buffers ({2 * w.fp8_layers} fp8 layers' K and V plus the bf16 attention layer) and "
+                            f"hidden rows [{w.B * w.N}][{inp.hidden.shape[1]}])")
         out["argmax_matches_planted_target"] = bool((arg.cpu().numpy() == inp.target_argmax).all())
     else:
         out["step_us"] = step_us
     del db, logits, ws, arg
     torch.cuda.empty_cache()
     return out
+
+
+def time_walk(db, stream, args):
+    """verify_tree_greedy alone (the walk over the step's links), CUDA-event
+    time per call; in the step it runs inside the fused epilogue."""
+    import torch
+    reps = max(5, min(args.steps, 50))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            db.walk_step(stream)
+        for r, (a, b) in enumerate(ev):
+            if r % AHEAD_STEPS == 0:
+                run_ahead(stream, 500.0)
+            a.record(stream)
+            db.walk_step(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    check_device_error(db, "the walk")
+    return statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
 
 
 def time_target_argmax(inp, db, stream, flush, args, hbm):

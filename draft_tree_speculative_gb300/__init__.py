@@ -28,7 +28,7 @@ EXPORTED = (
     "dts_tree_verify_attention_static_ws", "dts_target_argmax_workspace", "dts_target_argmax",
     "dts_verify_tree_greedy_logits", "dts_tree_window_attention_workspace", "dts_tree_window_attention",
     "dts_sample_draws", "dts_verify_tree_sampled", "dts_write_window_kv_fp8", "dts_tree_window_attention_fp8",
-    "dts_tree_verify_attention_fp8", "dts_test_stall_attention",
+    "dts_tree_verify_attention_fp8", "dts_test_stall_attention", "dts_verify_prologue", "dts_verify_epilogue",
 )
 
 
@@ -75,6 +75,9 @@ _SIGS = {
     "dts_compact_window_rows": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P]),
     "dts_compact_rows": (_I, [_P, _L, _P, _P, _P, _P, _I, _I, _P, _P]),
     "dts_test_stall_attention": (_I, [_I, ctypes.c_longlong]),
+    "dts_verify_prologue": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _L, _F, _P, _P, _P, _P, _P, _P,
+                                 _P, _P, _P]),
+    "dts_verify_epilogue": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _P, _P, _L, _P, _P, _P, _P]),
 }
 
 
@@ -492,3 +495,59 @@ def compact_rows(hidden, positions, vc, accepted_path, accept_len, err=None, str
     st = lib().dts_compact_rows(_ptr(hidden), row_bytes, _ptr(positions), _ptr(vc), _ptr(accepted_path),
                                 _ptr(accept_len), B, N, _ptr(err), _stream(stream))
     _raise(st, "compact_rows")
+
+
+def verify_prologue(parents, depth, vc, k_new, v_new, page_table, page_size, prefix_len, k_cache, v_cache, rope_theta,
+                    mask, positions, next_token, next_sibling, write_locations=None, err=None, stream=None):
+    """build_tree_mask and write_window_kv (bf16 cache) in one launch."""
+    torch = _torch()
+    B, N = parents.shape
+    BN, Hkv, d = k_new.shape
+    if BN != B * N:
+        raise ValueError("k_new must have B*N rows")
+    i32 = _i32()
+    _check(parents, i32, (B, N), "parents")
+    _check(depth, i32, (B, N), "depth")
+    _check(vc, i32, (B,), "vc")
+    _check(prefix_len, i32, (B,), "prefix_len")
+    _check(k_new, torch.bfloat16, (BN, Hkv, d), "k_new")
+    _check(v_new, torch.bfloat16, (BN, Hkv, d), "v_new")
+    _check(page_table, i32, None, "page_table")
+    _check(k_cache, torch.bfloat16, None, "k_cache")
+    _check(v_cache, torch.bfloat16, tuple(k_cache.shape), "v_cache")
+    _check(mask, _u64(), (B, N), "mask")
+    for name, t in (("positions", positions), ("next_token", next_token), ("next_sibling", next_sibling)):
+        _check(t, i32, (B, N), name)
+    _check(write_locations, torch.int64, (BN,), "write_locations")
+    st = lib().dts_verify_prologue(_ptr(parents), _ptr(depth), _ptr(vc), _ptr(k_new), _ptr(v_new), _ptr(page_table),
+                                   page_table.shape[1], page_size, _ptr(prefix_len), B, N, Hkv, d, k_cache.shape[0],
+                                   float(rope_theta), _ptr(mask), _ptr(positions), _ptr(next_token),
+                                   _ptr(next_sibling), _ptr(k_cache), _ptr(v_cache), _ptr(write_locations), _ptr(err),
+                                   _stream(stream))
+    _raise(st, "verify_prologue")
+
+
+def verify_epilogue(draft_tokens, target_argmax, accept_len, accepted_path, accepted_tokens, table=None,
+                    write_locations=None, hidden=None, positions=None, vc=None, parents=None, next_token=None,
+                    next_sibling=None, err=None, stream=None):
+    """verify_tree_greedy, compact_window_rows and compact_rows in one launch."""
+    B, N = draft_tokens.shape
+    i32 = _i32()
+    for name, t in (("draft_tokens", draft_tokens), ("target_argmax", target_argmax), ("parents", parents),
+                    ("next_token", next_token), ("next_sibling", next_sibling),
+                    ("accepted_path", accepted_path), ("accepted_tokens", accepted_tokens), ("positions", positions)):
+        _check(t, i32, (B, N), name)
+    _check(accept_len, i32, (B,), "accept_len")
+    _check(vc, i32, (B,), "vc")
+    _check(write_locations, _torch().int64, (B * N,), "write_locations")
+    row_bytes = 0
+    if hidden is not None:
+        row_bytes = hidden[0].numel() * hidden.element_size()
+        if hidden.shape[0] != B * N:
+            raise ValueError("hidden must have B*N rows")
+    n_buffers = 0 if table is None else table.shape[0]
+    st = lib().dts_verify_epilogue(_ptr(draft_tokens), _ptr(target_argmax), _ptr(parents), _ptr(next_token),
+                                   _ptr(next_sibling), B, N, _ptr(accept_len), _ptr(accepted_path),
+                                   _ptr(accepted_tokens), _ptr(table), n_buffers, _ptr(write_locations),
+                                   _ptr(hidden), row_bytes, _ptr(positions), _ptr(vc), _ptr(err), _stream(stream))
+    _raise(st, "verify_epilogue")

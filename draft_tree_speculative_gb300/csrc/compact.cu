@@ -1,263 +1,29 @@
-// Compaction of the accepted path: KV rows of every buffer in a cache group's
-// address table, and hidden rows plus positions.
-//
-// [TS] "The tree is a parameter of the chain path": the path's KV of every
-// layer moves to the window's leading slots by a word copy that does not care
-// about dtype, and the hidden rows move to the front of the window with the
-// positions back to vc + i. [MI] "Discarding the rejected branches' KV":
-// destinations are the first accept_len window slots.
-//
-// Snapshot order: the accepted path is strictly increasing with path[0] = 0,
-// so path[t] >= t. A row written for step t (window slot t) is never the
-// source of a later step t2 > t (whose source is slot path[t2] >= t2 > t).
-// The copy therefore runs in rounds over the moved rows in ascending order:
-// each round loads all of its words into registers, the block synchronises,
-// then stores them. Within a round every load precedes every store; across
-// rounds the argument above holds.
-#include "common.cuh"
+// Compaction entry points: the path's KV rows in every buffer of a cache
+// group's address table, and the hidden rows plus positions (the work itself
+// in compact.cuh).
+#include "compact.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kPerThread = 8;  // words staged per thread per round
+using dts::kBufPerBlock;
+using dts::kThreads;
 
-// Validate one request's packed path with one warp (lane l looks at steps l
-// and l + 32; N <= 64). Fills dst/src with the moved rows (in window-slot
-// units, ascending) and returns their count in every lane, or -1 for a bad
-// path.
-__device__ int collect_moves_warp(const int32_t *__restrict__ path, int alen, int N, int *dst, int *src) {
-  const int lane = threadIdx.x & 31;
-  if (alen < 1 || alen > N) return -1;
-  int n = 0;
-  bool bad = false;
-  int prev_hi = 0;  // path[31], the predecessor of step 32
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int t = half * 32 + lane;
-    const int p = t < alen ? path[t] : 0;
-    int before = __shfl_up_sync(0xffffffffu, p, 1);
-    if (lane == 0) before = prev_hi;
-    prev_hi = __shfl_sync(0xffffffffu, p, 31);
-    if (t < alen) {
-      if (t == 0) bad |= p != 0;
-      else bad |= p <= before || p >= N;
-    }
-    const bool moves = t >= 1 && t < alen && p != t;
-    const uint32_t m = __ballot_sync(0xffffffffu, moves);
-    if (moves) {
-      const int k = n + __popc(m & ((1u << lane) - 1u));
-      dst[k] = t;
-      src[k] = p;
-    }
-    n += __popc(m);
-  }
-  return __any_sync(0xffffffffu, bad) ? -1 : n;
-}
-
-template <typename Word>
-__device__ void move_rows(char *base, int64_t stride, int row_words, const int64_t *dst_slot,
-                          const int64_t *src_slot, int n_moved) {
-  const int64_t total = static_cast<int64_t>(n_moved) * row_words;
-  for (int64_t r0 = 0; r0 < total; r0 += static_cast<int64_t>(kThreads) * kPerThread) {
-    Word v[kPerThread];
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-      const int64_t e = r0 + static_cast<int64_t>(k) * kThreads + threadIdx.x;
-      if (e < total) {
-        const int m = static_cast<int>(e / row_words);
-        const int c = static_cast<int>(e % row_words);
-        v[k] = reinterpret_cast<const Word *>(base + src_slot[m] * stride)[c];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-      const int64_t e = r0 + static_cast<int64_t>(k) * kThreads + threadIdx.x;
-      if (e < total) {
-        const int m = static_cast<int>(e / row_words);
-        const int c = static_cast<int>(e % row_words);
-        reinterpret_cast<Word *>(base + dst_slot[m] * stride)[c] = v[k];
-      }
-    }
-    __syncthreads();
-  }
-}
-
-__device__ void move_rows_any(char *base, int64_t stride, int row_bytes, const int64_t *dst_slot,
-                              const int64_t *src_slot, int n_moved) {
-  const uint64_t a = reinterpret_cast<uint64_t>(base) | static_cast<uint64_t>(stride) |
-                     static_cast<uint64_t>(row_bytes);
-  if ((a & 15) == 0) move_rows<uint4>(base, stride, row_bytes / 16, dst_slot, src_slot, n_moved);
-  else if ((a & 7) == 0) move_rows<uint2>(base, stride, row_bytes / 8, dst_slot, src_slot, n_moved);
-  else move_rows<uint32_t>(base, stride, row_bytes / 4, dst_slot, src_slot, n_moved);
-}
-
-constexpr int kBufPerBlock = 8;  // buffers of the table one block moves
-
-// grid (ceil(n_buffers / kBufPerBlock), B): the request's moves are collected
-// once and applied to kBufPerBlock buffers; when every one of them is 16-byte
-// aligned, all their moved rows go in one load-then-store round.
+// grid (ceil(n_buffers / kBufPerBlock), B)
 __global__ void __launch_bounds__(kThreads) compact_window_rows_kernel(
     const dts_kv_buffer *__restrict__ table, int n_buffers, const int64_t *__restrict__ wl,
-    const int32_t *__restrict__ accepted_path, const int32_t *__restrict__ accept_len, int N,
-    int32_t *err) {
-  __shared__ int s_dst[dts::kMaxNodes], s_src[dts::kMaxNodes];
-  __shared__ int64_t s_dslot[dts::kMaxNodes], s_sslot[dts::kMaxNodes];
-  __shared__ dts_kv_buffer s_e[kBufPerBlock];
-  __shared__ int s_skip[kBufPerBlock];
-  __shared__ int64_t s_pref[kBufPerBlock + 1];  // words (16-byte) before buffer k's rows
-  __shared__ int s_n, s_all16;
-  const int l0 = blockIdx.x * kBufPerBlock;
-  const int nb = min(kBufPerBlock, n_buffers - l0);
+    const int32_t *__restrict__ accepted_path, const int32_t *__restrict__ accept_len, int N, int32_t *err) {
   const int b = blockIdx.y;
-  if (threadIdx.x < nb) {
-    const dts_kv_buffer e = table[l0 + threadIdx.x];
-    s_e[threadIdx.x] = e;
-    const uint64_t al = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
-                        static_cast<uint64_t>(e.row_bytes);
-    int skip = 0;
-    if (e.base == nullptr || (al & 3) != 0 || e.row_bytes <= 0 || e.slot_stride_bytes < e.row_bytes ||
-        e.num_slots <= 0 || e.reserved != 0) {
-      dts::report(err, DTS_DEV_BAD_BUFFER);
-      skip = 1;
-    }
-    s_skip[threadIdx.x] = skip;
-  }
-  __syncthreads();
-  // Each physical region moves once: skip an entry if another entry with the
-  // same stride covers its rows (equal ranges: the lower index moves).
-  for (int q = threadIdx.x; q < nb * n_buffers; q += kThreads) {
-    const int k = q / n_buffers, o = q - k * n_buffers;
-    const int l = l0 + k;
-    if (o == l || s_skip[k] == 1) continue;
-    const dts_kv_buffer e = s_e[k];
-    const dts_kv_buffer f = table[o];
-    if (f.slot_stride_bytes != e.slot_stride_bytes || f.base == nullptr) continue;
-    const uint64_t lo = reinterpret_cast<uint64_t>(e.base);
-    const uint64_t hi = lo + static_cast<uint64_t>(e.row_bytes);
-    const uint64_t flo = reinterpret_cast<uint64_t>(f.base);
-    const uint64_t fhi = flo + static_cast<uint64_t>(f.row_bytes);
-    if (fhi <= lo || hi <= flo) continue;                       // disjoint
-    const bool inside = flo <= lo && hi <= fhi;
-    const bool outside = lo <= flo && fhi <= hi;
-    if (inside && !(outside && o > l)) atomicOr(&s_skip[k], 2);  // covered by o
-    else if (!inside && !outside) atomicOr(&s_skip[k], 4);       // partial overlap
-  }
-  if (threadIdx.x < 32) {
-    const int n = collect_moves_warp(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
-    __syncwarp();
-    if (n < 0) {
-      if (threadIdx.x == 0) {
-        if (blockIdx.x == 0) dts::report(err, DTS_DEV_BAD_PATH);
-        s_n = 0;
-      }
-    } else {
-      for (int m = threadIdx.x; m < n; m += 32) {
-        s_dslot[m] = wl[static_cast<int64_t>(b) * N + s_dst[m]];
-        s_sslot[m] = wl[static_cast<int64_t>(b) * N + s_src[m]];
-      }
-      if (threadIdx.x == 0) s_n = n;
-    }
-  }
-  __syncthreads();
-  const int n_moved = s_n;
-  if (n_moved == 0) return;
-  if (threadIdx.x < nb) {
-    // slots in range for this buffer, the overlap verdicts, 16-byte words
-    const dts_kv_buffer e = s_e[threadIdx.x];
-    int skip = s_skip[threadIdx.x];
-    if (skip & 4) {
-      if (b == 0) dts::report(err, DTS_DEV_BAD_BUFFER);
-    }
-    if (skip == 0) {
-      bool bad = false;
-      for (int m = 0; m < n_moved; ++m)
-        bad |= s_dslot[m] < 0 || s_dslot[m] >= e.num_slots || s_sslot[m] < 0 || s_sslot[m] >= e.num_slots;
-      if (bad) {
-        dts::report(err, DTS_DEV_BAD_SLOT);
-        skip = 8;
-      }
-    }
-    s_skip[threadIdx.x] = skip;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int64_t acc = 0;
-    int all16 = 1;
-    for (int k = 0; k < nb; ++k) {
-      s_pref[k] = acc;
-      if (s_skip[k] != 0) continue;
-      const dts_kv_buffer e = s_e[k];
-      const uint64_t al = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
-                          static_cast<uint64_t>(e.row_bytes);
-      all16 &= (al & 15) == 0 ? 1 : 0;
-      acc += static_cast<int64_t>(n_moved) * (e.row_bytes / 16);
-    }
-    s_pref[nb] = acc;
-    s_all16 = all16;
-  }
-  __syncthreads();
-  if (!s_all16) {
-    for (int k = 0; k < nb; ++k)
-      if (s_skip[k] == 0)
-        move_rows_any(static_cast<char *>(s_e[k].base), s_e[k].slot_stride_bytes, s_e[k].row_bytes, s_dslot,
-                      s_sslot, n_moved);
-    return;
-  }
-  // every moved row of every buffer, as 16-byte words, in rounds
-  const int64_t total = s_pref[nb];
-  for (int64_t r0 = 0; r0 < total; r0 += static_cast<int64_t>(kThreads) * kPerThread) {
-    uint4 v[kPerThread];
-    char *dst_addr[kPerThread];
-#pragma unroll
-    for (int q = 0; q < kPerThread; ++q) {
-      const int64_t e = r0 + static_cast<int64_t>(q) * kThreads + threadIdx.x;
-      dst_addr[q] = nullptr;
-      if (e < total) {
-        int k = 0;
-        while (k + 1 < nb && s_pref[k + 1] <= e) ++k;
-        const int64_t row_words = s_e[k].row_bytes / 16;
-        const int64_t local = e - s_pref[k];
-        const int m = static_cast<int>(local / row_words);
-        const int64_t c = local - m * row_words;
-        char *base = static_cast<char *>(s_e[k].base);
-        v[q] = reinterpret_cast<const uint4 *>(base + s_sslot[m] * s_e[k].slot_stride_bytes)[c];
-        dst_addr[q] = base + s_dslot[m] * s_e[k].slot_stride_bytes + c * 16;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < kPerThread; ++q)
-      if (dst_addr[q] != nullptr) *reinterpret_cast<uint4 *>(dst_addr[q]) = v[q];
-    __syncthreads();
-  }
+  dts::compact_kv_block(table, n_buffers, blockIdx.x, wl, accepted_path + static_cast<int64_t>(b) * N, accept_len[b],
+                        b, N, err);
 }
 
 // grid (B)
 __global__ void __launch_bounds__(kThreads) compact_rows_kernel(
-    char *__restrict__ hidden, int64_t row_bytes, int32_t *__restrict__ positions,
-    const int32_t *__restrict__ vc, const int32_t *__restrict__ accepted_path,
-    const int32_t *__restrict__ accept_len, int N, int32_t *err) {
-  __shared__ int s_dst[dts::kMaxNodes], s_src[dts::kMaxNodes];
-  __shared__ int64_t s_dslot[dts::kMaxNodes], s_sslot[dts::kMaxNodes];
-  __shared__ int s_n;
+    char *__restrict__ hidden, int64_t row_bytes, int32_t *__restrict__ positions, const int32_t *__restrict__ vc,
+    const int32_t *__restrict__ accepted_path, const int32_t *__restrict__ accept_len, int N, int32_t *err) {
   const int b = blockIdx.x;
-  if (positions != nullptr)
-    for (int i = threadIdx.x; i < N; i += kThreads) positions[static_cast<int64_t>(b) * N + i] = vc[b] + i;
-  if (hidden == nullptr) return;
-  if (threadIdx.x < 32) {
-    const int n = collect_moves_warp(accepted_path + static_cast<int64_t>(b) * N, accept_len[b], N, s_dst, s_src);
-    __syncwarp();
-    if (n < 0 && threadIdx.x == 0) dts::report(err, DTS_DEV_BAD_PATH);
-    for (int m = threadIdx.x; m < n; m += 32) {
-      s_dslot[m] = static_cast<int64_t>(b) * N + s_dst[m];
-      s_sslot[m] = static_cast<int64_t>(b) * N + s_src[m];
-    }
-    if (threadIdx.x == 0) s_n = n < 0 ? 0 : n;
-  }
-  __syncthreads();
-  if (s_n == 0) return;
-  move_rows_any(hidden, row_bytes, static_cast<int>(row_bytes), s_dslot, s_sslot, s_n);
+  dts::compact_hidden_block(hidden, row_bytes, positions, vc, accepted_path + static_cast<int64_t>(b) * N,
+                            hidden != nullptr ? accept_len[b] : 0, b, N, err);
 }
 
 }  // namespace

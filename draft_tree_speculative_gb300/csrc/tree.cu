@@ -6,7 +6,7 @@
 //   ancestors), [MI] "Flattening, and the two link arrays".
 // verify_tree_greedy: one warp per request. [MI] "Walking the accepted path";
 //   [AK] section two (accept_len = correct drafts + 1, bonus = last argmax).
-#include "common.cuh"
+#include "walk.cuh"
 
 namespace {
 
@@ -68,105 +68,20 @@ __global__ void __launch_bounds__(64) build_tree_mask_kernel(
   next_sibling[row] = sibling;
 }
 
-// One warp per request; each lane owns nodes `lane` and `lane + 32`.
-// parent/rank of every node are derived from the links (or from parents), so
-// the walk is: among the children of `cur` whose draft equals argmax[cur],
-// take the lowest rank (first in sibling order), via one warp min-reduction
-// per accepted level.
+// One warp per request (the walk itself in walk.cuh).
 __global__ void __launch_bounds__(128) verify_tree_greedy_kernel(
     const int32_t *__restrict__ draft, const int32_t *__restrict__ argmax,
     const int32_t *__restrict__ parents, const int32_t *__restrict__ next_token,
     const int32_t *__restrict__ next_sibling, int B, int N, int32_t *__restrict__ accept_len,
     int32_t *__restrict__ accepted_path, int32_t *__restrict__ accepted_tokens, int32_t *err) {
   constexpr int kWarps = 4;
-  __shared__ int s_par[kWarps][kMaxNodes];
-  __shared__ int s_rank[kWarps][kMaxNodes];
-  __shared__ int s_arg[kWarps][kMaxNodes];
-  __shared__ int s_path[kWarps][kMaxNodes];
+  __shared__ dts::WalkScratch s_walk[kWarps];
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * kWarps + w;
   if (b >= B) return;
-  const int64_t base = static_cast<int64_t>(b) * N;
-  int *par = s_par[w];
-  int *rank = s_rank[w];
-  int *arg = s_arg[w];
-  int *path = s_path[w];
-
-  int my_draft[2];
-  for (int k = 0; k < 2; ++k) {
-    const int j = lane + 32 * k;
-    my_draft[k] = 0;
-    if (j < N) {
-      my_draft[k] = draft[base + j];
-      arg[j] = argmax[base + j];
-      par[j] = -2;  // "not a child of anything yet"
-      rank[j] = 0;
-    }
-  }
-  __syncwarp();
-  bool bad = false;
-  if (next_token != nullptr) {
-    // Each lane walks the child lists of its own nodes.
-    for (int k = 0; k < 2; ++k) {
-      const int p = lane + 32 * k;
-      if (p >= N) continue;
-      int c = next_token[base + p];
-      int r = 0;
-      while (c != -1) {
-        if (c <= 0 || c >= N || r >= N) {  // the root is nobody's child
-          bad = true;
-          break;
-        }
-        if (atomicCAS(&par[c], -2, p) != -2) {  // a node on two lists, or a cycle
-          bad = true;
-          break;
-        }
-        rank[c] = r++;
-        c = next_sibling[base + c];
-      }
-    }
-  } else {
-    for (int k = 0; k < 2; ++k) {
-      const int j = lane + 32 * k;
-      if (j >= N) continue;
-      const int p = parents[base + j];
-      if (j == 0 ? p != -1 : (p < 0 || p >= j)) bad = true;
-      par[j] = (j == 0) ? -2 : p;
-      rank[j] = j;
-    }
-  }
-  __syncwarp();
-  bad = __any_sync(0xffffffffu, bad);
-  if (bad && lane == 0) dts::report(err, next_token != nullptr ? DTS_DEV_BAD_LINK : DTS_DEV_BAD_PARENT);
-
-  int cur = 0, len = 1;
-  if (lane == 0) path[0] = 0;
-  if (!bad) {
-    for (int step = 1; step < N; ++step) {
-      const int target = arg[cur];
-      unsigned best = 0xFFFFFFFFu;
-      for (int k = 0; k < 2; ++k) {
-        const int j = lane + 32 * k;
-        if (j < N && par[j] == cur && my_draft[k] == target)
-          best = min(best, (static_cast<unsigned>(rank[j]) << 8) | static_cast<unsigned>(j));
-      }
-      best = __reduce_min_sync(0xffffffffu, best);
-      if (best == 0xFFFFFFFFu) break;
-      cur = static_cast<int>(best & 0xFFu);
-      if (lane == 0) path[len] = cur;
-      ++len;
-    }
-  }
-  __syncwarp();
-  for (int k = 0; k < 2; ++k) {
-    const int t = lane + 32 * k;
-    if (t >= N) continue;
-    const int node = t < len ? path[t] : -1;
-    accepted_path[base + t] = node;
-    accepted_tokens[base + t] = node >= 0 ? arg[node] : -1;
-  }
-  if (lane == 0) accept_len[b] = len;
+  const int len = dts::greedy_walk_warp(draft, argmax, parents, next_token, next_sibling, b, N, s_walk[w], lane, err);
+  dts::write_walk_outputs(s_walk[w], len, b, N, lane, accept_len, accepted_path, accepted_tokens);
 }
 
 }  // namespace

@@ -7,6 +7,9 @@ path in order:
   build_tree_mask -> write_window_kv -> tree_verify_attention
   -> verify_tree_greedy -> compact_window_rows -> compact_rows
 
+by default as three calls: verify_prologue (the first two), the attention,
+verify_epilogue (the last three).
+
 (the caller's logits/argmax sit between the attention and the walk; the
 synthetic batch provides target_argmax directly). All calls go to one CUDA
 stream; nothing synchronises inside a step.
@@ -19,7 +22,8 @@ import numpy as np
 
 from . import synth
 from . import (build_tree_mask, write_window_kv, tree_verify_attention, tree_verify_attention_workspace,
-               verify_tree_greedy, compact_window_rows, compact_rows, make_kv_table)
+               verify_tree_greedy, compact_window_rows, compact_rows, make_kv_table, verify_prologue,
+               verify_epilogue)
 
 
 def _torch():
@@ -36,7 +40,7 @@ def bf16_tensor(bits: np.ndarray, device):
 class DeviceBatch:
     """Device-resident inputs, outputs and scratch of one verify step."""
 
-    KERNELS_PER_STEP = 8  # mask, window kv, attention prep, tree attention, merge, walk, KV compaction, row compaction
+    KERNELS_PER_STEP = 5  # prologue, attention prep, tree attention, merge, epilogue
 
     def __init__(self, inp: synth.VerifyInputs, device="cuda", fp8_layers: Optional[int] = None,
                  compact_attention_kv: bool = True):
@@ -118,6 +122,20 @@ class DeviceBatch:
                            self.accepted_tokens, next_token=self.next_token, next_sibling=self.next_sibling,
                            err=self.err, stream=stream)
 
+    # the fused launches: mask + window K/V, and walk + both compactions
+    def prologue_step(self, stream=None):
+        verify_prologue(self.parents, self.depth, self.vc, self.k_new, self.v_new, self.page_table, self.page_size,
+                        self.prefix_len, self.k_cache, self.v_cache, self.w.rope_theta, self.mask, self.positions,
+                        self.next_token, self.next_sibling, write_locations=self.write_locations, err=self.err,
+                        stream=stream)
+
+    def epilogue_step(self, stream=None, target_argmax=None):
+        verify_epilogue(self.draft, self.target_argmax if target_argmax is None else target_argmax, self.accept_len,
+                        self.accepted_path, self.accepted_tokens, table=self.kv_table,
+                        write_locations=self.write_locations, hidden=self.hidden, positions=self.positions,
+                        vc=self.vc, next_token=self.next_token, next_sibling=self.next_sibling, err=self.err,
+                        stream=stream)
+
     def compact_step(self, stream=None):
         if self.kv_table is not None:
             compact_window_rows(self.kv_table, self.write_locations, self.accepted_path, self.accept_len,
@@ -126,8 +144,15 @@ class DeviceBatch:
                      stream=stream)
 
 
-def run_step(db: DeviceBatch, stream=None, compact: bool = True):
-    """One pass of the whole hot path; returns nothing (outputs stay on the device)."""
+def run_step(db: DeviceBatch, stream=None, compact: bool = True, fused: bool = True):
+    """One pass of the whole hot path; returns nothing (outputs stay on the
+    device). fused: the prologue (mask + window K/V) and epilogue (walk +
+    compactions) launches; otherwise the separate calls."""
+    if fused and compact:
+        db.prologue_step(stream)
+        db.attention_step(stream)
+        db.epilogue_step(stream)
+        return
     db.mask_step(stream)
     db.window_kv_step(stream)
     db.attention_step(stream)

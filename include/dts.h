@@ -508,6 +508,63 @@ int dts_compact_rows(void *hidden, int64_t row_bytes, int32_t *positions, const 
                      int32_t *err_dev, dts_stream_t stream);
 
 /*
+ * dts_verify_prologue - dts_build_tree_mask and dts_write_window_kv (bf16
+ * cache) in one launch, one warp per node. Each warp validates its request's
+ * tree, forms its node's ancestor mask, position vc + depth, first child and
+ * next sibling, and writes the node's rotated K and its V to the node's
+ * window slot. The outputs, their layouts and the device-side errors are
+ * exactly those of the two calls made in turn (with prefix_len for the slots
+ * and vc for the positions, as there); arguments are validated as for those
+ * calls.
+ *
+ *   parents, depth, vc            as for dts_build_tree_mask
+ *   k_new, v_new, page_table, max_pages, page_size, prefix_len, Hkv, d,
+ *   num_slots, rope_theta, k_cache, v_cache, write_locations
+ *                                 as for dts_write_window_kv
+ *   mask, positions, next_token, next_sibling   out, as for dts_build_tree_mask
+ *
+ * Sources as for the two calls ([TS] "One tree attention", "Position follows
+ * depth, slot follows node index"; [AK] section one; [MI] "Building the mask,
+ * for real", "Flattening, and the two link arrays").
+ */
+int dts_verify_prologue(const int32_t *parents, const int32_t *depth, const int32_t *vc,
+                        const uint16_t *k_new, const uint16_t *v_new, const int32_t *page_table,
+                        int max_pages, int page_size, const int32_t *prefix_len, int B, int N,
+                        int Hkv, int d, int64_t num_slots, float rope_theta, uint64_t *mask,
+                        int32_t *positions, int32_t *next_token, int32_t *next_sibling,
+                        uint16_t *k_cache, uint16_t *v_cache, int64_t *write_locations,
+                        int32_t *err_dev, dts_stream_t stream);
+
+/*
+ * dts_verify_epilogue - dts_verify_tree_greedy, dts_compact_window_rows and
+ * dts_compact_rows in one launch: one block per (request, group of 8 KV
+ * buffers); the block's first warp walks the request's tree, and the block
+ * moves that request's KV rows (its group of the table) along the accepted
+ * path; the first block of each request also moves the hidden rows and
+ * resets the positions. The outputs and device-side errors are exactly those
+ * of the three calls made in turn with the walk's outputs; arguments are
+ * validated as for those calls.
+ *
+ *   draft_tokens, target_argmax, parents, next_token, next_sibling,
+ *   accept_len, accepted_path, accepted_tokens
+ *                                 as for dts_verify_tree_greedy
+ *   table, n_buffers, write_locations   as for dts_compact_window_rows
+ *                                 (n_buffers = 0: no KV rows move)
+ *   hidden, row_bytes, positions, vc    as for dts_compact_rows
+ *
+ * Sources as for the three calls ([MI] "Walking the accepted path",
+ * "Discarding the rejected branches' KV"; [AK] section two; [TS] "The tree is
+ * a parameter of the chain path").
+ */
+int dts_verify_epilogue(const int32_t *draft_tokens, const int32_t *target_argmax,
+                        const int32_t *parents, const int32_t *next_token,
+                        const int32_t *next_sibling, int B, int N, int32_t *accept_len,
+                        int32_t *accepted_path, int32_t *accepted_tokens,
+                        const dts_kv_buffer *table, int n_buffers, const int64_t *write_locations,
+                        void *hidden, int64_t row_bytes, int32_t *positions, const int32_t *vc,
+                        int32_t *err_dev, dts_stream_t stream);
+
+/*
  * dts_test_stall_attention - test hook, not a step of the verify path (the
  * pages have no counterpart). It lets a test make the tensor-core tree pass
  * give up on purpose, without a fault: with stall = 1, the pass's producer

@@ -149,3 +149,27 @@ def test_stall_hook_validates(lib):
     assert L.dts_test_stall_attention(1, 100) == dts.ERR_INVALID
     assert L.dts_test_stall_attention(1, 1 << 40) == dts.ERR_INVALID
     assert L.dts_test_stall_attention(0, 1 << 31) == dts.OK
+
+
+def test_fused_step_calls_validate(lib):
+    """The fused prologue and epilogue refuse what the separate calls refuse,
+    before any launch; B = 0 launches nothing."""
+    L = dts.lib()
+    pro = lambda B=1, N=8, d=128, ps=64, theta=5e5, ptr=None: L.dts_verify_prologue(
+        ptr, ptr, ptr, ptr, ptr, ptr, 4, ps, ptr, B, N, 8, d, 100, theta, ptr, ptr, ptr, ptr, ptr, ptr, None, None,
+        None)
+    assert pro(N=65) == dts.ERR_UNSUPPORTED
+    assert pro(d=96) == dts.ERR_UNSUPPORTED
+    assert pro(ps=48) == dts.ERR_UNSUPPORTED
+    assert pro(theta=0.0) == dts.ERR_INVALID
+    assert pro(B=0) == dts.OK
+    assert pro() == dts.ERR_INVALID                      # null pointers
+    assert pro(ptr=4100) == dts.ERR_INVALID              # K/V not 8-byte aligned
+    epi = lambda B=1, N=8, nb=0, links=True, ptr=None: L.dts_verify_epilogue(
+        ptr, ptr, None, ptr if links else None, ptr if links else None, B, N, ptr, ptr, ptr, ptr, nb, ptr, None, 0,
+        None, None, None, None)
+    assert epi(N=65) == dts.ERR_UNSUPPORTED
+    assert epi(B=0) == dts.OK
+    assert epi() == dts.ERR_INVALID                      # null pointers
+    assert epi(ptr=4096, links=False) == dts.ERR_INVALID  # neither links nor parents
+    assert epi(ptr=4096, nb=-1) == dts.ERR_INVALID
