@@ -62,7 +62,7 @@ struct Plan {
   int64_t o_off, lse_off, tb_off, q_off, total;
 };
 
-// Workspace: partial O [slots][slot_rows][d] fp32 | partial LSE
+// Workspace: partial O [slots][slot_rows][d] bf16 | partial LSE
 // [slots][slot_rows] fp32 | tiles-before table [B+1] int64 | rotated queries
 // [B*N][Hq][d] bf16. A slot holds one unit's rows (at most two row tiles).
 Plan make_plan(int B, int R, int Hq, int Hkv, int d) {
@@ -76,7 +76,7 @@ Plan make_plan(int B, int R, int Hq, int Hkv, int d) {
   p.units = static_cast<int64_t>(B) * Hkv * p.n_pairs;
   p.slots = p.units + kMaxGrid;
   p.o_off = 0;
-  p.lse_off = align_up(p.o_off + p.slots * p.slot_rows * d * 4, 256);
+  p.lse_off = align_up(p.o_off + p.slots * p.slot_rows * d * 2, 256);
   p.tb_off = align_up(p.lse_off + p.slots * p.slot_rows * 4, 256);
   p.q_off = align_up(p.tb_off + (static_cast<int64_t>(B) + 1) * 8, 256);
   p.total = align_up(p.q_off + static_cast<int64_t>(B) * R * Hq * d * 2, 256);
@@ -193,7 +193,7 @@ struct PrefixArgs {
   const int32_t *page_table;
   const int32_t *prefix_len;
   const uint64_t *mask;
-  float *o_part;
+  uint16_t *o_part;  // bf16 partial rows
   float *lse_part;
   int64_t *tiles_before;  // [B + 1], written by CTA 0 for the merge pass
   uint16_t *out;
@@ -1026,26 +1026,29 @@ __global__ void __launch_bounds__(384, 1)
         // combines the unit's partials)
         const int64_t slot_row = (static_cast<int64_t>(sg.unit) + blockIdx.x) * a.slot_rows + prow;
         if (warp_valid) {
-          // Thread = row, and a row of the partial is 4 D contiguous bytes:
-          // stored straight, every 16-byte store would hit another row, and
-          // the epilogue runs at the rate of partial-sector writes. So each
-          // 8-lane group transposes its 8 rows x 8 float4 units of a 32-column
-          // chunk (three xor-butterfly stages) and then writes one row's 128
-          // contiguous bytes per store.
+          // The partial row is normalised and stored in bf16, like the
+          // output: its extra rounding (2^-9 relative) sits far inside the
+          // output's tolerance and halves the bytes every split unit writes
+          // here and the merge pass reads back. Thread = row, and a row is 2 D
+          // contiguous bytes: stored straight, every store would hit another
+          // row, and the epilogue would run at the rate of partial-sector
+          // writes. So each 8-lane group transposes its 8 rows x 8 units (8
+          // bytes = 4 columns) of a 32-column chunk (three xor-butterfly
+          // stages) and then writes one row's 64 contiguous bytes per store.
           const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
           const int grp = lane & ~7, cu = lane & 7;
-          float *dst0 = a.o_part + (slot_row - cu) * D + 4 * cu;  // row grp + 0, this lane's unit
+          uint16_t *dst0 = a.o_part + (slot_row - cu) * D + 4 * cu;  // row grp + 0, this lane's unit
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
             uint32_t ov[32];
             tmem_ld32(tO + q * 32, ov);
             tmem_wait_ld();
-            float4 u[8];
+            uint2 u[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              u[k] = make_float4(__uint_as_float(ov[4 * k]) * inv_l, __uint_as_float(ov[4 * k + 1]) * inv_l,
-                                 __uint_as_float(ov[4 * k + 2]) * inv_l, __uint_as_float(ov[4 * k + 3]) * inv_l);
-              if (poisoned) u[k] = make_float4(NAN, NAN, NAN, NAN);
+              u[k].x = dts::pack_bf16x2(__uint_as_float(ov[4 * k]) * inv_l, __uint_as_float(ov[4 * k + 1]) * inv_l);
+              u[k].y = dts::pack_bf16x2(__uint_as_float(ov[4 * k + 2]) * inv_l, __uint_as_float(ov[4 * k + 3]) * inv_l);
+              if (poisoned) u[k] = make_uint2(0x7FC07FC0u, 0x7FC07FC0u);
             }
 #pragma unroll
             for (int mi = 0; mi < 3; ++mi) {
@@ -1054,12 +1057,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
                 if (k & m) continue;
-                const float4 snd = hi ? u[k] : u[k | m];
-                float4 rcv;
+                const uint2 snd = hi ? u[k] : u[k | m];
+                uint2 rcv;
                 rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
                 rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
-                rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
-                rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
                 if (hi) u[k] = rcv;
                 else u[k | m] = rcv;
               }
@@ -1067,7 +1068,7 @@ __global__ void __launch_bounds__(384, 1)
             // this lane now holds unit cu of rows grp .. grp + 7
 #pragma unroll
             for (int r = 0; r < 8; ++r)
-              if ((vmask >> (grp + r)) & 1u) *reinterpret_cast<float4 *>(dst0 + r * D + q * 32) = u[r];
+              if ((vmask >> (grp + r)) & 1u) *reinterpret_cast<uint2 *>(dst0 + r * D + q * 32) = u[r];
           }
           if (valid) a.lse_part[slot_row] = lse_row;
         }
@@ -1100,7 +1101,7 @@ __global__ void __launch_bounds__(384, 1)
 // merge pass
 // ============================================================================
 struct MergeArgs {
-  const float *o_part;
+  const uint16_t *o_part;  // bf16 partial rows
   const float *lse_part;
   const int64_t *tiles_before;
   const int32_t *prefix_len;
@@ -1260,21 +1261,22 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       if (((live >> (8 * k)) & 0xFFu) == 0u) continue;
-      const float *base = a.o_part + ((static_cast<int64_t>(unit) + c0 + k) * a.slot_rows + rb * kRows) * D + E * lane;
+      const uint16_t *base =
+          a.o_part + ((static_cast<int64_t>(unit) + c0 + k) * a.slot_rows + rb * kRows) * D + E * lane;
       float x[kRows][E];
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
         if (rb * kRows + i < a.slot_rows) {
           if constexpr (E == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(base + i * D);
-            x[i][0] = v.x;
-            x[i][1] = v.y;
-            x[i][2] = v.z;
-            x[i][3] = v.w;
+            const uint2 v = *reinterpret_cast<const uint2 *>(base + i * D);
+            x[i][0] = dts::bf16_lo(v.x);
+            x[i][1] = dts::bf16_hi(v.x);
+            x[i][2] = dts::bf16_lo(v.y);
+            x[i][3] = dts::bf16_hi(v.y);
           } else {
-            const float2 v = *reinterpret_cast<const float2 *>(base + i * D);
-            x[i][0] = v.x;
-            x[i][1] = v.y;
+            const uint32_t v = *reinterpret_cast<const uint32_t *>(base + i * D);
+            x[i][0] = dts::bf16_lo(v);
+            x[i][1] = dts::bf16_hi(v);
           }
         } else {
 #pragma unroll
@@ -1461,7 +1463,7 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   const Plan plan = make_plan(B, R, Hq, Hkv, d);
   if (workspace == nullptr || ws_bytes < static_cast<size_t>(plan.total)) return DTS_ERR_WORKSPACE;
   char *ws = static_cast<char *>(workspace);
-  float *o_part = reinterpret_cast<float *>(ws + plan.o_off);
+  uint16_t *o_part = reinterpret_cast<uint16_t *>(ws + plan.o_off);
   float *lse_part = reinterpret_cast<float *>(ws + plan.lse_off);
   int64_t *tiles_before = reinterpret_cast<int64_t *>(ws + plan.tb_off);
   uint16_t *q_rot = reinterpret_cast<uint16_t *>(ws + plan.q_off);
