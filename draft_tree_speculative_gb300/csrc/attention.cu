@@ -107,6 +107,8 @@ struct PrepArgs {
 // Consecutive threads take consecutive chunks of a row (coalesced 16-byte loads).
 template <int D>
 __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ PrepArgs a) {
+  dts::grid_dep_wait();
+  dts::grid_dep_launch_next();
   constexpr int kChunks = D / 16;
   constexpr int kMaxHeads = 4;
   const int hgroups = a.Hq / a.heads_per_thread;
@@ -459,6 +461,8 @@ template <int D, bool F8>
 __global__ void __launch_bounds__(384, 1)
     tree_prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ PrefixArgs a) {
+  dts::grid_dep_wait();
+  dts::grid_dep_launch_next();
   using S = PrefixShape<D>;
   constexpr int kSlots = S::kSlots;
   constexpr uint32_t kTileBytes = S::kTileBytes;
@@ -1200,6 +1204,8 @@ __device__ bool window_part_f8(const MergeArgs &a, int b, int hkv, int P, uint64
 // once whether its group owns tiles; the row loads of the four parts follow.
 template <int D, bool F8>
 __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__ MergeArgs a) {
+  dts::grid_dep_wait();
+  dts::grid_dep_launch_next();
   constexpr int kRows = 8;
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
@@ -1418,7 +1424,7 @@ int launch_prefix(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMa
                                     static_cast<int>(S::kSmem));
   });
   if (attr_err != cudaSuccess) return DTS_ERR_CUDA;
-  tree_prefix_kernel<D, F8><<<grid, S::kThreads, S::kSmem, s>>>(tk, tv, tq, a);
+  dts_host::launch_chained(tree_prefix_kernel<D, F8>, dim3(grid), dim3(S::kThreads), S::kSmem, s, tk, tv, tq, a);
   return dts_host::launch_status();
 }
 
@@ -1493,8 +1499,8 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
     if (positions != nullptr) dts_host::make_rope_freqs(rope_theta, d, &ra.freqs);
     const int64_t items = static_cast<int64_t>(B) * R * (Hq / ra.heads_per_thread) * (d / 16);
     const int blocks = static_cast<int>((items + 255) / 256);
-    if (d == 128) attn_prep_kernel<128><<<blocks, 256, 0, s>>>(ra);
-    else attn_prep_kernel<64><<<blocks, 256, 0, s>>>(ra);
+    if (d == 128) dts_host::launch_chained(attn_prep_kernel<128>, dim3(blocks), dim3(256), 0, s, ra);
+    else dts_host::launch_chained(attn_prep_kernel<64>, dim3(blocks), dim3(256), 0, s, ra);
     if (dts_host::launch_status() != DTS_OK) return DTS_ERR_CUDA;
   }
   const uint16_t *q_eff = (positions != nullptr || f8) ? q_rot : q;
@@ -1579,9 +1585,9 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   }
   const int64_t warps = plan.units * ((plan.slot_rows + 7) / 8);
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  if (f8) tree_merge_kernel<128, true><<<blocks, 256, 0, s>>>(ma);
-  else if (d == 128) tree_merge_kernel<128, false><<<blocks, 256, 0, s>>>(ma);
-  else tree_merge_kernel<64, false><<<blocks, 256, 0, s>>>(ma);
+  if (f8) dts_host::launch_chained(tree_merge_kernel<128, true>, dim3(blocks), dim3(256), 0, s, ma);
+  else if (d == 128) dts_host::launch_chained(tree_merge_kernel<128, false>, dim3(blocks), dim3(256), 0, s, ma);
+  else dts_host::launch_chained(tree_merge_kernel<64, false>, dim3(blocks), dim3(256), 0, s, ma);
   return dts_host::launch_status();
 }
 

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dts.h"
 
 namespace dts {
@@ -18,6 +20,18 @@ constexpr int kMaxNodes = 64;
 __device__ __forceinline__ void report(int32_t *err, int code) {
   if (err != nullptr) atomicCAS(reinterpret_cast<int *>(err), 0, code);
 }
+
+// Programmatic dependent launch. A kernel of the verify step may be launched
+// before the kernel ahead of it in the stream has finished (launch_chained
+// below), so its launch and block scheduling overlap that kernel's tail.
+// grid_dep_wait() blocks until the kernel ahead has completed and its memory
+// operations are visible; every such kernel calls it before it touches
+// global memory. grid_dep_launch_next() lets the next kernel in the stream
+// be launched once every block of this grid has issued it (or exited); its
+// blocks then wait in their own grid_dep_wait(). Both are no-ops for a
+// kernel launched the ordinary way.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_next() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -94,6 +108,24 @@ __device__ __forceinline__ void rope_sincos(int pos, float2 w, float *s, float *
 
 // Host helpers (defined in api.cu).
 namespace dts_host {
+// Launches `kernel` on stream `s` with programmatic stream serialization: it
+// may start while the kernel ahead of it in the stream is still running and
+// must call dts::grid_dep_wait() before its first global-memory access.
+template <typename... Params, typename... Args>
+cudaError_t launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                           Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 void make_rope_freqs(float theta, int d, dts::RopeFreqs *out);
 int launch_status();  // DTS_OK or DTS_ERR_CUDA from cudaGetLastError()
 int sm_count();

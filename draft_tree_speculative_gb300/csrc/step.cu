@@ -42,6 +42,8 @@ __device__ __forceinline__ int node_value(int v0, int v1, int j) {
 
 template <int D>
 __global__ void __launch_bounds__(256) verify_prologue_kernel(const __grid_constant__ PrologueArgs a) {
+  dts::grid_dep_wait();
+  dts::grid_dep_launch_next();
   const int node = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // b * N + i
   const int lane = threadIdx.x & 31;
   const int B = a.kv.B, N = a.kv.N;
@@ -117,6 +119,8 @@ struct EpilogueArgs {
 
 // grid (max(1, ceil(n_buffers / kBufPerBlock)), B)
 __global__ void __launch_bounds__(dts::kThreads) verify_epilogue_kernel(const __grid_constant__ EpilogueArgs a) {
+  dts::grid_dep_wait();
+  dts::grid_dep_launch_next();
   __shared__ dts::WalkScratch ws;
   __shared__ int s_len;
   const int b = blockIdx.y, gx = blockIdx.x;
@@ -181,8 +185,8 @@ extern "C" int dts_verify_prologue(const int32_t *parents, const int32_t *depth,
   const int64_t warps = static_cast<int64_t>(B) * N;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (d == 128) verify_prologue_kernel<128><<<blocks, 256, 0, s>>>(a);
-  else verify_prologue_kernel<64><<<blocks, 256, 0, s>>>(a);
+  if (d == 128) dts_host::launch_chained(verify_prologue_kernel<128>, dim3(blocks), dim3(256), 0, s, a);
+  else dts_host::launch_chained(verify_prologue_kernel<64>, dim3(blocks), dim3(256), 0, s, a);
   return dts_host::launch_status();
 }
 
@@ -224,6 +228,7 @@ extern "C" int dts_verify_epilogue(const int32_t *draft_tokens, const int32_t *t
   a.err = err_dev;
   a.N = N;
   const int groups = n_buffers > 0 ? (n_buffers + dts::kBufPerBlock - 1) / dts::kBufPerBlock : 1;
-  verify_epilogue_kernel<<<dim3(groups, B), dts::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  dts_host::launch_chained(verify_epilogue_kernel, dim3(groups, B), dim3(dts::kThreads), 0,
+                           reinterpret_cast<cudaStream_t>(stream), a);
   return dts_host::launch_status();
 }

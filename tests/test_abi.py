@@ -136,8 +136,8 @@ def test_static_workspace_validates_like_the_regular_call(lib):
         assert reg == sta == want, (kw, reg, sta)
     # a shape beyond the static array is refused as a workspace error once the
     # arguments are valid (aligned non-null pointers; nothing is launched)
-    big = dict(B=32, N=64, ptr=4096)
-    assert dts.tree_verify_attention_workspace(32, 64, 32, 8, 128, 0) > (64 << 20)
+    big = dict(B=64, N=64, ptr=4096)
+    assert dts.tree_verify_attention_workspace(64, 64, 32, 8, 128, 0) > (64 << 20)
     assert both(**big) == (dts.ERR_WORKSPACE, dts.ERR_WORKSPACE)
 
 

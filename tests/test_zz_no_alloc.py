@@ -28,7 +28,7 @@ def _static_call(db, out, lse2):
                                         err=db.err, N=db.N)
 
 
-@pytest.mark.parametrize("name", ["llama8b_p4096_n8", "highconc_b128_n16"])
+@pytest.mark.parametrize("name", ["llama8b_p4096_n8", "eagle2_p8192_n64", "highconc_b128_n16"])
 def test_static_workspace_matches_caller_workspace(name):
     torch = torch_cuda()
     inp = synth.make_inputs(synth.WORKLOADS[name], with_hidden=False)
@@ -59,11 +59,12 @@ def test_static_workspace_matches_caller_workspace(name):
 
 def test_static_workspace_refuses_shapes_beyond_its_size():
     torch = torch_cuda()
-    w = synth.WORKLOADS["eagle2_p8192_n64"]       # needs more than 64 MiB of workspace
-    assert dts.tree_verify_attention_workspace(w.B, w.N, w.Hq, w.Hkv, w.d, 8192) > (64 << 20)
+    w = synth.WORKLOADS["eagle2_p8192_n64"]
+    B = 2 * w.B                                   # twice eagle2's batch needs more than 64 MiB
+    assert dts.tree_verify_attention_workspace(B, w.N, w.Hq, w.Hkv, w.d, 8192) > (64 << 20)
     L = dts.lib()
     buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")   # valid pointers; nothing is launched
     p = buf.data_ptr()
-    st = L.dts_tree_verify_attention_static_ws(p, p, p, 1 << 20, p, 200, 64, p, 8192, p, p, 5e5, w.B, w.N, w.Hq,
+    st = L.dts_tree_verify_attention_static_ws(p, p, p, 1 << 20, p, 200, 64, p, 8192, p, p, 5e5, B, w.N, w.Hq,
                                                w.Hkv, w.d, 0.0, p, p, None, torch.cuda.current_stream().cuda_stream)
     assert st == dts.ERR_WORKSPACE
