@@ -12,9 +12,11 @@ using dts::kThreads;
 __global__ void __launch_bounds__(kThreads) compact_window_rows_kernel(
     const dts_kv_buffer *__restrict__ table, int n_buffers, const int64_t *__restrict__ wl,
     const int32_t *__restrict__ accepted_path, const int32_t *__restrict__ accept_len, int N, int32_t *err) {
+  __shared__ dts::KvCompactSmem kv;
   const int b = blockIdx.y;
-  dts::compact_kv_block(table, n_buffers, blockIdx.x, wl, accepted_path + static_cast<int64_t>(b) * N, accept_len[b],
-                        b, N, err);
+  dts::kv_prepare(table, n_buffers, blockIdx.x, wl, b, N, kv, threadIdx.x, kThreads);
+  __syncthreads();
+  dts::kv_move(n_buffers, blockIdx.x, accepted_path + static_cast<int64_t>(b) * N, accept_len[b], b, N, kv, err);
 }
 
 // grid (B)
@@ -22,8 +24,9 @@ __global__ void __launch_bounds__(kThreads) compact_rows_kernel(
     char *__restrict__ hidden, int64_t row_bytes, int32_t *__restrict__ positions, const int32_t *__restrict__ vc,
     const int32_t *__restrict__ accepted_path, const int32_t *__restrict__ accept_len, int N, int32_t *err) {
   const int b = blockIdx.x;
-  dts::compact_hidden_block(hidden, row_bytes, positions, vc, accepted_path + static_cast<int64_t>(b) * N,
-                            hidden != nullptr ? accept_len[b] : 0, b, N, err);
+  dts::write_positions(positions, vc, b, N, threadIdx.x, kThreads);
+  dts::move_hidden_block(hidden, row_bytes, accepted_path + static_cast<int64_t>(b) * N,
+                         hidden != nullptr ? accept_len[b] : 0, b, N, err);
 }
 
 }  // namespace

@@ -97,118 +97,135 @@ __device__ __forceinline__ void move_rows_any(char *base, int64_t stride, int ro
 
 constexpr int kBufPerBlock = 8;  // buffers of the table one block moves
 
-// One block moves request b's path rows in buffers [gx * kBufPerBlock, ...)
-// of the table: the request's moves are collected once and applied to
-// kBufPerBlock buffers; when every one of them is 16-byte aligned, all their
-// moved rows go in one load-then-store round. `path` points at the request's
-// packed path (global or shared memory), `alen` is its length.
-__device__ __forceinline__ void compact_kv_block(const dts_kv_buffer *__restrict__ table, int n_buffers, int gx,
-                                                 const int64_t *__restrict__ wl, const int32_t *path, int alen,
-                                                 int b, int N, int32_t *err) {
-  __shared__ int s_dst[kMaxNodes], s_src[kMaxNodes];
-  __shared__ int64_t s_dslot[kMaxNodes], s_sslot[kMaxNodes];
-  __shared__ dts_kv_buffer s_e[kBufPerBlock];
-  __shared__ int s_skip[kBufPerBlock];
-  __shared__ int64_t s_pref[kBufPerBlock + 1];  // words (16-byte) before buffer k's rows
-  __shared__ int s_n, s_all16;
+// Shared state of one block's KV compaction (kv_prepare, then kv_move).
+struct KvCompactSmem {
+  int dst[kMaxNodes], src[kMaxNodes];        // moved rows, in window-slot units
+  int64_t dslot[kMaxNodes], sslot[kMaxNodes];
+  int64_t wl[kMaxNodes];                      // the request's window slots
+  dts_kv_buffer e[kBufPerBlock];
+  int skip[kBufPerBlock];
+  int64_t pref[kBufPerBlock + 1];             // words (16-byte) before buffer k's rows
+  int n, all16;
+};
+
+// The part of request b's KV compaction in buffers [gx * kBufPerBlock, ...)
+// of the table that does not need its path: the buffers' entries and their
+// checks, the overlap verdicts between entries, and the request's window
+// slots. Threads tid = 0 .. nthr - 1 of the block take part, whole warps,
+// nthr a multiple of 32 (the rest may be walking the tree meanwhile); they
+// meet once on hardware barrier 1. Nothing is reported yet, and the caller
+// synchronises the block before kv_move.
+__device__ __forceinline__ void kv_prepare(const dts_kv_buffer *__restrict__ table, int n_buffers, int gx,
+                                           const int64_t *__restrict__ wl, int b, int N, KvCompactSmem &s, int tid,
+                                           int nthr) {
   const int l0 = gx * kBufPerBlock;
   const int nb = min(kBufPerBlock, n_buffers - l0);
-  if (threadIdx.x < nb) {
-    const dts_kv_buffer e = table[l0 + threadIdx.x];
-    s_e[threadIdx.x] = e;
+  for (int k = tid; k < nb; k += nthr) {
+    const dts_kv_buffer e = table[l0 + k];
+    s.e[k] = e;
     const uint64_t al = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
                         static_cast<uint64_t>(e.row_bytes);
-    int skip = 0;
-    if (e.base == nullptr || (al & 3) != 0 || e.row_bytes <= 0 || e.slot_stride_bytes < e.row_bytes ||
-        e.num_slots <= 0 || e.reserved != 0) {
-      report(err, DTS_DEV_BAD_BUFFER);
-      skip = 1;
-    }
-    s_skip[threadIdx.x] = skip;
+    const bool bad = e.base == nullptr || (al & 3) != 0 || e.row_bytes <= 0 || e.slot_stride_bytes < e.row_bytes ||
+                     e.num_slots <= 0 || e.reserved != 0;
+    s.skip[k] = bad ? 1 : 0;
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
   // Each physical region moves once: skip an entry if another entry with the
   // same stride covers its rows (equal ranges: the lower index moves).
-  for (int q = threadIdx.x; q < nb * n_buffers; q += kThreads) {
+  for (int q = tid; q < nb * n_buffers; q += nthr) {
     const int k = q / n_buffers, o = q - k * n_buffers;
     const int l = l0 + k;
-    if (o == l || s_skip[k] == 1) continue;
-    const dts_kv_buffer e = s_e[k];
+    if (o == l || s.skip[k] == 1) continue;
+    const dts_kv_buffer e = s.e[k];
     const dts_kv_buffer f = table[o];
     if (f.slot_stride_bytes != e.slot_stride_bytes || f.base == nullptr) continue;
     const uint64_t lo = reinterpret_cast<uint64_t>(e.base);
     const uint64_t hi = lo + static_cast<uint64_t>(e.row_bytes);
     const uint64_t flo = reinterpret_cast<uint64_t>(f.base);
     const uint64_t fhi = flo + static_cast<uint64_t>(f.row_bytes);
-    if (fhi <= lo || hi <= flo) continue;                       // disjoint
+    if (fhi <= lo || hi <= flo) continue;                     // disjoint
     const bool inside = flo <= lo && hi <= fhi;
     const bool outside = lo <= flo && fhi <= hi;
-    if (inside && !(outside && o > l)) atomicOr(&s_skip[k], 2);  // covered by o
-    else if (!inside && !outside) atomicOr(&s_skip[k], 4);       // partial overlap
+    if (inside && !(outside && o > l)) atomicOr(&s.skip[k], 2);  // covered by o
+    else if (!inside && !outside) atomicOr(&s.skip[k], 4);       // partial overlap
   }
+  for (int j = tid; j < N; j += nthr) s.wl[j] = wl[static_cast<int64_t>(b) * N + j];
+}
+
+// The rest, once kv_prepare's writes are visible to the block: request b's
+// path rows move in the prepared buffers. `path` points at the request's
+// packed path (global or shared memory), `alen` is its length. When every
+// buffer is 16-byte aligned, all their moved rows go in one load-then-store
+// round. Errors are reported in the order the checks are defined: a bad
+// entry, a bad path, a partial overlap, a slot out of range.
+__device__ __forceinline__ void kv_move(int n_buffers, int gx, const int32_t *path, int alen, int b, int N,
+                                        KvCompactSmem &s, int32_t *err) {
+  const int nb = min(kBufPerBlock, n_buffers - gx * kBufPerBlock);
+  if (threadIdx.x < nb && s.skip[threadIdx.x] == 1) report(err, DTS_DEV_BAD_BUFFER);
+  __syncthreads();
   if (threadIdx.x < 32) {
-    const int n = collect_moves_warp(path, alen, N, s_dst, s_src);
+    const int n = collect_moves_warp(path, alen, N, s.dst, s.src);
     __syncwarp();
     if (n < 0) {
       if (threadIdx.x == 0) {
         if (gx == 0) report(err, DTS_DEV_BAD_PATH);
-        s_n = 0;
+        s.n = 0;
       }
     } else {
       for (int m = threadIdx.x; m < n; m += 32) {
-        s_dslot[m] = wl[static_cast<int64_t>(b) * N + s_dst[m]];
-        s_sslot[m] = wl[static_cast<int64_t>(b) * N + s_src[m]];
+        s.dslot[m] = s.wl[s.dst[m]];
+        s.sslot[m] = s.wl[s.src[m]];
       }
-      if (threadIdx.x == 0) s_n = n;
+      if (threadIdx.x == 0) s.n = n;
     }
   }
   __syncthreads();
-  const int n_moved = s_n;
+  const int n_moved = s.n;
   if (n_moved == 0) return;
   if (threadIdx.x < nb) {
     // slots in range for this buffer, the overlap verdicts, 16-byte words
-    const dts_kv_buffer e = s_e[threadIdx.x];
-    int skip = s_skip[threadIdx.x];
+    const dts_kv_buffer e = s.e[threadIdx.x];
+    int skip = s.skip[threadIdx.x];
     if (skip & 4) {
       if (b == 0) report(err, DTS_DEV_BAD_BUFFER);
     }
     if (skip == 0) {
       bool bad = false;
       for (int m = 0; m < n_moved; ++m)
-        bad |= s_dslot[m] < 0 || s_dslot[m] >= e.num_slots || s_sslot[m] < 0 || s_sslot[m] >= e.num_slots;
+        bad |= s.dslot[m] < 0 || s.dslot[m] >= e.num_slots || s.sslot[m] < 0 || s.sslot[m] >= e.num_slots;
       if (bad) {
         report(err, DTS_DEV_BAD_SLOT);
         skip = 8;
       }
     }
-    s_skip[threadIdx.x] = skip;
+    s.skip[threadIdx.x] = skip;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int64_t acc = 0;
     int all16 = 1;
     for (int k = 0; k < nb; ++k) {
-      s_pref[k] = acc;
-      if (s_skip[k] != 0) continue;
-      const dts_kv_buffer e = s_e[k];
+      s.pref[k] = acc;
+      if (s.skip[k] != 0) continue;
+      const dts_kv_buffer e = s.e[k];
       const uint64_t al = reinterpret_cast<uint64_t>(e.base) | static_cast<uint64_t>(e.slot_stride_bytes) |
                           static_cast<uint64_t>(e.row_bytes);
       all16 &= (al & 15) == 0 ? 1 : 0;
       acc += static_cast<int64_t>(n_moved) * (e.row_bytes / 16);
     }
-    s_pref[nb] = acc;
-    s_all16 = all16;
+    s.pref[nb] = acc;
+    s.all16 = all16;
   }
   __syncthreads();
-  if (!s_all16) {
+  if (!s.all16) {
     for (int k = 0; k < nb; ++k)
-      if (s_skip[k] == 0)
-        move_rows_any(static_cast<char *>(s_e[k].base), s_e[k].slot_stride_bytes, s_e[k].row_bytes, s_dslot,
-                      s_sslot, n_moved);
+      if (s.skip[k] == 0)
+        move_rows_any(static_cast<char *>(s.e[k].base), s.e[k].slot_stride_bytes, s.e[k].row_bytes, s.dslot,
+                      s.sslot, n_moved);
     return;
   }
   // every moved row of every buffer, as 16-byte words, in rounds
-  const int64_t total = s_pref[nb];
+  const int64_t total = s.pref[nb];
   for (int64_t r0 = 0; r0 < total; r0 += static_cast<int64_t>(kThreads) * kPerThread) {
     uint4 v[kPerThread];
     char *dst_addr[kPerThread];
@@ -218,14 +235,14 @@ __device__ __forceinline__ void compact_kv_block(const dts_kv_buffer *__restrict
       dst_addr[q] = nullptr;
       if (e < total) {
         int k = 0;
-        while (k + 1 < nb && s_pref[k + 1] <= e) ++k;
-        const int64_t row_words = s_e[k].row_bytes / 16;
-        const int64_t local = e - s_pref[k];
+        while (k + 1 < nb && s.pref[k + 1] <= e) ++k;
+        const int64_t row_words = s.e[k].row_bytes / 16;
+        const int64_t local = e - s.pref[k];
         const int m = static_cast<int>(local / row_words);
         const int64_t c = local - m * row_words;
-        char *base = static_cast<char *>(s_e[k].base);
-        v[q] = reinterpret_cast<const uint4 *>(base + s_sslot[m] * s_e[k].slot_stride_bytes)[c];
-        dst_addr[q] = base + s_dslot[m] * s_e[k].slot_stride_bytes + c * 16;
+        char *base = static_cast<char *>(s.e[k].base);
+        v[q] = reinterpret_cast<const uint4 *>(base + s.sslot[m] * s.e[k].slot_stride_bytes)[c];
+        dst_addr[q] = base + s.dslot[m] * s.e[k].slot_stride_bytes + c * 16;
       }
     }
     __syncthreads();
@@ -236,16 +253,21 @@ __device__ __forceinline__ void compact_kv_block(const dts_kv_buffer *__restrict
   }
 }
 
+// Request b's positions back to vc + i (threads tid = 0 .. nthr - 1).
+__device__ __forceinline__ void write_positions(int32_t *__restrict__ positions, const int32_t *__restrict__ vc,
+                                                int b, int N, int tid, int nthr) {
+  if (positions == nullptr) return;
+  const int v = vc[b];
+  for (int i = tid; i < N; i += nthr) positions[static_cast<int64_t>(b) * N + i] = v + i;
+}
+
 // One block: request b's hidden rows along its path (global or shared
-// `path`, length `alen`) and its positions back to vc + i.
-__device__ __forceinline__ void compact_hidden_block(char *__restrict__ hidden, int64_t row_bytes,
-                                                     int32_t *__restrict__ positions, const int32_t *__restrict__ vc,
-                                                     const int32_t *path, int alen, int b, int N, int32_t *err) {
+// `path`, length `alen`).
+__device__ __forceinline__ void move_hidden_block(char *__restrict__ hidden, int64_t row_bytes, const int32_t *path,
+                                                  int alen, int b, int N, int32_t *err) {
   __shared__ int s_dst[kMaxNodes], s_src[kMaxNodes];
   __shared__ int64_t s_dslot[kMaxNodes], s_sslot[kMaxNodes];
   __shared__ int s_n;
-  if (positions != nullptr)
-    for (int i = threadIdx.x; i < N; i += kThreads) positions[static_cast<int64_t>(b) * N + i] = vc[b] + i;
   if (hidden == nullptr) return;
   if (threadIdx.x < 32) {
     const int n = collect_moves_warp(path, alen, N, s_dst, s_src);

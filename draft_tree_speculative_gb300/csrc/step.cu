@@ -115,28 +115,39 @@ struct EpilogueArgs {
   const int32_t *vc;
   int32_t *err;
   int N;
+  int kv_groups;  // blocks per request that move KV rows
 };
 
-// grid (max(1, ceil(n_buffers / kBufPerBlock)), B)
+// grid (kv_groups + 1, B). Every block walks request b with warp 0 (the path
+// lands in shared memory). Meanwhile the other warps of block gx < kv_groups
+// stage what the KV move of buffer group gx needs short of the path (the
+// entries, their checks, the window slots), and those of the last block write
+// the positions; then block gx moves its KV rows, and the last block writes the
+// walk's outputs and moves the hidden rows.
 __global__ void __launch_bounds__(dts::kThreads) verify_epilogue_kernel(const __grid_constant__ EpilogueArgs a) {
   dts::grid_dep_wait();
   dts::grid_dep_launch_next();
   __shared__ dts::WalkScratch ws;
+  __shared__ dts::KvCompactSmem kv;
   __shared__ int s_len;
   const int b = blockIdx.y, gx = blockIdx.x;
+  const bool rows_block = gx == a.kv_groups;
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int len =
         dts::greedy_walk_warp(a.draft, a.argmax, a.parents, a.next_token, a.next_sibling, b, a.N, ws, lane, a.err);
-    if (gx == 0)
+    if (rows_block)
       dts::write_walk_outputs(ws, len, b, a.N, lane, a.accept_len, a.accepted_path, a.accepted_tokens);
     if (lane == 0) s_len = len;
+  } else if (!rows_block) {
+    dts::kv_prepare(a.table, a.n_buffers, gx, a.write_locations, b, a.N, kv, threadIdx.x - 32, dts::kThreads - 32);
+  } else {
+    dts::write_positions(a.positions, a.vc, b, a.N, threadIdx.x - 32, dts::kThreads - 32);
   }
   __syncthreads();
   const int alen = s_len;
-  if (a.n_buffers > 0) dts::compact_kv_block(a.table, a.n_buffers, gx, a.write_locations, ws.path, alen, b, a.N, a.err);
-  __syncthreads();
-  if (gx == 0) dts::compact_hidden_block(a.hidden, a.row_bytes, a.positions, a.vc, ws.path, alen, b, a.N, a.err);
+  if (!rows_block) dts::kv_move(a.n_buffers, gx, ws.path, alen, b, a.N, kv, a.err);
+  else dts::move_hidden_block(a.hidden, a.row_bytes, ws.path, alen, b, a.N, a.err);
 }
 
 }  // namespace
@@ -227,8 +238,8 @@ extern "C" int dts_verify_epilogue(const int32_t *draft_tokens, const int32_t *t
   a.vc = vc;
   a.err = err_dev;
   a.N = N;
-  const int groups = n_buffers > 0 ? (n_buffers + dts::kBufPerBlock - 1) / dts::kBufPerBlock : 1;
-  dts_host::launch_chained(verify_epilogue_kernel, dim3(groups, B), dim3(dts::kThreads), 0,
+  a.kv_groups = (n_buffers + dts::kBufPerBlock - 1) / dts::kBufPerBlock;
+  dts_host::launch_chained(verify_epilogue_kernel, dim3(a.kv_groups + 1, B), dim3(dts::kThreads), 0,
                            reinterpret_cast<cudaStream_t>(stream), a);
   return dts_host::launch_status();
 }
