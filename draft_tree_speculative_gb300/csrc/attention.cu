@@ -59,12 +59,13 @@ int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 struct Plan {
   int g, npt, rt, n_pairs, slot_rows;
   int64_t units, slots;
-  int64_t o_off, lse_off, tb_off, q_off, total;
+  int64_t o_off, lse_off, tb_off, cnt_off, q_off, total;
 };
 
 // Workspace: partial O [slots][slot_rows][d] bf16 | partial LSE
-// [slots][slot_rows] fp32 | tiles-before table [B+1] int64 | rotated queries
-// [B*N][Hq][d] bf16. A slot holds one unit's rows (at most two row tiles).
+// [slots][slot_rows] fp32 | tiles-before table [B+1] int64 | parts stored
+// per unit [units] int32 | rotated queries [B*N][Hq][d] bf16. A slot holds
+// one unit's rows (at most two row tiles).
 Plan make_plan(int B, int R, int Hq, int Hkv, int d) {
   Plan p;
   p.g = Hq / Hkv;
@@ -78,7 +79,8 @@ Plan make_plan(int B, int R, int Hq, int Hkv, int d) {
   p.o_off = 0;
   p.lse_off = align_up(p.o_off + p.slots * p.slot_rows * d * 2, 256);
   p.tb_off = align_up(p.lse_off + p.slots * p.slot_rows * 4, 256);
-  p.q_off = align_up(p.tb_off + (static_cast<int64_t>(B) + 1) * 8, 256);
+  p.cnt_off = align_up(p.tb_off + (static_cast<int64_t>(B) + 1) * 8, 256);
+  p.q_off = align_up(p.cnt_off + p.units * 4, 256);
   p.total = align_up(p.q_off + static_cast<int64_t>(B) * R * Hq * d * 2, 256);
   return p;
 }
@@ -99,6 +101,8 @@ struct PrepArgs {
   int rows, R, W, Hq, heads_per_thread;   // rows = B*R query rows; W window keys per request
   int to_e4m3;  // FP8 cache: store the (rotated, bf16-rounded) queries as E4M3 bytes, and the
                 // bf16 ones in `out` (read back there by the merge pass for the window keys)
+  int32_t *unit_cnt;  // [units] zeroed here for the tree pass's merge (null: none)
+  int64_t units;
   dts::RopeFreqs freqs;
 };
 
@@ -113,6 +117,8 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
   constexpr int kMaxHeads = 4;
   const int hgroups = a.Hq / a.heads_per_thread;
   const int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (a.unit_cnt != nullptr)
+    for (int64_t u = it; u < a.units; u += static_cast<int64_t>(gridDim.x) * blockDim.x) a.unit_cnt[u] = 0;
   if (it >= static_cast<int64_t>(a.rows) * hgroups * kChunks) return;
   const int c = static_cast<int>(it % kChunks);
   const int hg = static_cast<int>((it / kChunks) % hgroups);
@@ -189,6 +195,230 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const __grid_constant__ 
 }
 
 // ============================================================================
+// merge pass
+// ============================================================================
+struct MergeArgs {
+  const uint16_t *o_part;  // bf16 partial rows
+  const float *lse_part;
+  const int64_t *tiles_before;
+  const int32_t *prefix_len;
+  uint16_t *out;
+  float *lse2;
+  int64_t max_prefix, capacity;
+  int B, R, W, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;  // W: window keys of the tree pass
+  int owners32;  // every (tile index + 1) * groups fits in 32 bits
+  // F8 only: the window part, from the bf16 rotated queries the prep pass
+  // left in `out`, the mask and the E4M3 window K/V in the paged cache
+  const uint64_t *mask;
+  const uint8_t *k8, *v8;
+  const int32_t *page_table;
+  int32_t *err;
+  int64_t num_slots;
+  int Ww, max_pages, page_shift;  // Ww: window keys of the window part
+  float scale_log2;
+};
+
+// Which group's range holds flat tile x, and whether group c owns any tile:
+// the tree pass gives group c the tiles [c T / G, (c + 1) T / G).
+struct Owners {
+  int64_t T, G;
+  bool w32;
+  __device__ int64_t of(int64_t x) const {  // ((x + 1) G - 1) / T
+    if (w32) return (static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(G) - 1u) / static_cast<uint32_t>(T);
+    return ((x + 1) * G - 1) / T;
+  }
+  __device__ bool owns(int64_t c) const {
+    if (w32) {
+      const uint32_t t = static_cast<uint32_t>(T), g = static_cast<uint32_t>(G), c32 = static_cast<uint32_t>(c);
+      return c32 * t / g < (c32 + 1u) * t / g;
+    }
+    return c * T / G < (c + 1) * T / G;
+  }
+};
+
+// F8 window part of one row: the row's visible window keys (bits of `bits`)
+// scored against its bf16 rotated query q[] (this lane's E columns) with the
+// E4M3 K rows widened exactly, an online softmax in base 2 (m, l) and the
+// unnormalised sum of the widened V rows in o[]. A non-finite K or V row
+// turns the rows that see it NaN. Returns false (after reporting) when a
+// window slot lies outside the cache; the row then reads NaN.
+template <int D>
+__device__ bool window_part_f8(const MergeArgs &a, int b, int hkv, int P, uint64_t bits, const float (&q)[D / 32],
+                               int lane, float &m, float &l, float (&o)[D / 32]) {
+  constexpr int E = D / 32;
+  static_assert(E == 4, "the E4M3 cache takes d = 128");
+  m = -INFINITY;
+  l = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  const int ps = 1 << a.page_shift;
+  while (bits != 0ull) {
+    const int j = __ffsll(static_cast<long long>(bits)) - 1;
+    bits &= bits - 1ull;
+    const int pos = P + j;
+    const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
+    const int64_t slot = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
+    if (page < 0 || slot >= a.num_slots) {
+      if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
+      return false;
+    }
+    const int64_t off = (slot * a.Hkv + hkv) * D + E * lane;
+    const uint32_t kw = *reinterpret_cast<const uint32_t *>(a.k8 + off);
+    const uint32_t vw = *reinterpret_cast<const uint32_t *>(a.v8 + off);
+    const uint32_t k01 = dts::e4m3x2_to_f16x2(kw & 0xFFFFu), k23 = dts::e4m3x2_to_f16x2(kw >> 16);
+    const uint32_t v01 = dts::e4m3x2_to_f16x2(vw & 0xFFFFu), v23 = dts::e4m3x2_to_f16x2(vw >> 16);
+    const float k[4] = {dts::f16_lo(k01), dts::f16_hi(k01), dts::f16_lo(k23), dts::f16_hi(k23)};
+    const float v[4] = {dts::f16_lo(v01), dts::f16_hi(v01), dts::f16_lo(v23), dts::f16_hi(v23)};
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dot = fmaf(q[e], k[e], dot);
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+    const float sc = dot * a.scale_log2;
+    const float m_new = fmaxf(m, sc);  // (a NaN score leaves m; its weight below is NaN)
+    const float corr = m == -INFINITY ? 0.f : exp2f(m - m_new);
+    const float p = sc == -INFINITY ? 0.f : exp2f(sc - m_new);
+    l = l * corr + p;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = o[e] * corr + p * v[e];
+    m = m_new;
+  }
+  return true;
+}
+
+// The merge of rows [8 rb, 8 rb + 8) of unit `unit` (row pair `pair`, request
+// b, KV head hkv, prefix length P) by one warp, from the parts left by the
+// groups c_first .. c_last of the tree pass.
+template <int D, bool F8>
+__device__ __forceinline__ void merge_rows(const MergeArgs &a, uint32_t unit, int rb, int pair, int b, int hkv, int P,
+                                           int64_t c_first, int64_t c_last, const Owners &own, int lane) {
+  constexpr int kRows = 8;
+  constexpr int E = D / 32;
+  const int i_row = lane & 7;
+  const int prow_l = rb * kRows + i_row;
+  const bool row_ok = prow_l < a.slot_rows;
+  const int64_t row0 = static_cast<int64_t>(unit) * a.slot_rows + prow_l;  // this lane's row in slot `unit`
+
+  // pass 1: the largest LSE of each row (the first four parts' LSEs are kept)
+  float lse_first = -INFINITY;
+  float mx = -INFINITY;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    const int64_t c = c0 + (lane >> 3);
+    float lse = -INFINITY;
+    if (c <= c_last && row_ok && own.owns(c)) lse = __ldcg(a.lse_part + row0 + c * a.slot_rows);
+    if (c0 == c_first) lse_first = lse;
+    mx = fmaxf(mx, lse);
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  // pass 2: weights, their sum and the weighted rows
+  float acc[kRows][E];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
+  float den = 0.f;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    const int64_t c = c0 + (lane >> 3);
+    float lse = lse_first;
+    if (c0 != c_first) {
+      lse = -INFINITY;
+      if (c <= c_last && row_ok && own.owns(c)) lse = __ldcg(a.lse_part + row0 + c * a.slot_rows);
+    }
+    const float w = lse == -INFINITY ? 0.f : dts::ptx::ex2(lse - mx);  // a part that saw no key drops out
+    den += w;
+    // which of the four parts have rows to read (warp-uniform): a part whose
+    // weights are all 0 (not a group with tiles, or no key seen) is skipped
+    const uint32_t live = __ballot_sync(0xffffffffu, w != 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (((live >> (8 * k)) & 0xFFu) == 0u) continue;
+      const uint16_t *base =
+          a.o_part + ((static_cast<int64_t>(unit) + c0 + k) * a.slot_rows + rb * kRows) * D + E * lane;
+      float x[kRows][E];
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        if (rb * kRows + i < a.slot_rows) {
+          if constexpr (E == 4) {
+            const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(base + i * D));
+            x[i][0] = dts::bf16_lo(v.x);
+            x[i][1] = dts::bf16_hi(v.x);
+            x[i][2] = dts::bf16_lo(v.y);
+            x[i][3] = dts::bf16_hi(v.y);
+          } else {
+            const uint32_t v = __ldcg(reinterpret_cast<const unsigned int *>(base + i * D));
+            x[i][0] = dts::bf16_lo(v);
+            x[i][1] = dts::bf16_hi(v);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) x[i][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, k * 8 + i);
+        if (wi == 0.f) continue;  // warp-uniform
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[i][e] = fmaf(x[i][e], wi, acc[i][e]);
+      }
+    }
+  }
+  den += __shfl_xor_sync(0xffffffffu, den, 8);
+  den += __shfl_xor_sync(0xffffffffu, den, 16);
+
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int prow = rb * kRows + i;
+    float den_i = __shfl_sync(0xffffffffu, den, i);
+    float mx_i = __shfl_sync(0xffffffffu, mx, i);
+    const int R = pair * 2 * a.rt + prow;  // row of the KV head
+    if (prow >= a.slot_rows || R >= a.M) continue;
+    const int node = R / a.g;
+    const int64_t node_row = static_cast<int64_t>(b) * a.R + node;
+    const int64_t out_row = node_row * a.Hq + hkv * a.g + (R - node * a.g);
+    float num[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) num[e] = acc[i][e];
+    if constexpr (F8) {
+      // the window part: the prefix parts (lse mx_i, weight den_i) and the
+      // window keys (max m_w, weight l_w) meet at their common maximum
+      float q[E];
+      if constexpr (E == 4) {
+        const uint2 qw = *reinterpret_cast<const uint2 *>(a.out + out_row * D + E * lane);
+        q[0] = dts::bf16_lo(qw.x);
+        q[1] = dts::bf16_hi(qw.x);
+        q[2] = dts::bf16_lo(qw.y);
+        q[3] = dts::bf16_hi(qw.y);
+      }
+      const uint64_t bits = a.mask[node_row] & (a.Ww < 64 ? (1ull << a.Ww) - 1ull : ~0ull);
+      float m_w, l_w, o_w[E];
+      bool slot_ok = true;
+      if constexpr (E == 4) slot_ok = window_part_f8<D>(a, b, hkv, P, bits, q, lane, m_w, l_w, o_w);
+      const float M2 = fmaxf(mx_i, m_w);
+      const float ap = mx_i == -INFINITY ? 0.f : exp2f(mx_i - M2);
+      const float aw = m_w == -INFINITY ? 0.f : exp2f(m_w - M2);
+#pragma unroll
+      for (int e = 0; e < E; ++e) num[e] = ap * num[e] + aw * o_w[e];
+      den_i = ap * den_i + aw * l_w;
+      mx_i = M2;
+      if (!slot_ok) den_i = __int_as_float(0x7FC00000);
+    }
+    const float inv = den_i == 0.f ? 0.f : 1.f / den_i;  // (a NaN sum stays NaN)
+    if constexpr (E == 4) {
+      uint2 v;
+      v.x = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
+      v.y = dts::pack_bf16x2(num[2] * inv, num[3] * inv);
+      *reinterpret_cast<uint2 *>(a.out + out_row * D + E * lane) = v;
+    } else {
+      *reinterpret_cast<uint32_t *>(a.out + out_row * D + E * lane) = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
+    }
+    if (lane == 0) a.lse2[out_row] = den_i == 0.f ? -INFINITY : mx_i + __log2f(den_i);
+  }
+}
+
+
+// ============================================================================
 // tree attention
 // ============================================================================
 struct PrefixArgs {
@@ -198,6 +428,7 @@ struct PrefixArgs {
   uint16_t *o_part;  // bf16 partial rows
   float *lse_part;
   int64_t *tiles_before;  // [B + 1], written by CTA 0 for the merge pass
+  int32_t *unit_cnt;      // [units] parts of each unit stored so far (zeroed by prep); null: no merge here
   uint16_t *out;
   float *lse2;
   int32_t *err;
@@ -206,6 +437,15 @@ struct PrefixArgs {
   float scale_log2;
   long long wait_budget;  // cycles before a bounded wait gives up
   int stall;              // test hook: the producer issues no copy at all
+  int owners32;           // every (tile index + 1) * grid fits in 32 bits
+};
+
+// A unit whose last part this CTA stored: the softmax groups merge it at the
+// end of the pass.
+struct MergeEntry {
+  int64_t c_first, c_last;
+  uint32_t unit;
+  int pair, b, hkv, P, pad;
 };
 
 template <int D>
@@ -216,8 +456,9 @@ struct PrefixShape {
   static constexpr int kSlots = D == 128 ? 5 : 8;      // K/V ring
   static constexpr uint32_t kBarBytes = 512;
   // kfull, vfull, empty, vready rings, 10 single barriers, two poison masks,
-  // the tile total (two words) and the TMEM address / abort flag words
-  static_assert((4 * kSlots + 10) * 8 + 16 + 16 + 8 <= kBarBytes, "barrier area too small");
+  // then from the tile total on: 2 words for it, the TMEM address, the abort
+  // flag and 3 counters (within 4 words), and 2 merge entries
+  static_assert((4 * kSlots + 10) * 8 + 16 + 6 * 8 + 2 * sizeof(MergeEntry) <= kBarBytes, "barrier area too small");
   static constexpr uint32_t kSmem = 1024 /*align*/ + 2 * kTileBytes + kSlots * kTileBytes + kBarBytes;
 };
 
@@ -319,6 +560,9 @@ __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu
 __device__ __forceinline__ uint32_t p_bar_id(int t, int r) {
   return 1u + 2u * static_cast<uint32_t>(t) + (static_cast<uint32_t>(r) & 1u);
 }
+// The eight softmax warps meet once more, on their own barrier, before they
+// merge the units whose last part the CTA stored.
+constexpr uint32_t kMergeBarrier = 5;
 
 // Phase of use u on a barrier that only the slot's uses of u's kind (K: even
 // uses, V: odd ones) complete: with an even ring a slot holds the same kind
@@ -493,6 +737,10 @@ __global__ void __launch_bounds__(384, 1)
   int64_t *range = reinterpret_cast<int64_t *>(poison + 2);  // [0] = total tiles
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(range + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // [0], [1]: warps of the CTA's first / last partial segment that stored
+  // their rows; [2]: entries in the merge list
+  int *part_cnt = const_cast<int *>(abort_flag) + 1;
+  MergeEntry *mlist = reinterpret_cast<MergeEntry *>(range + 6);  // [2]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -513,6 +761,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int s2 = 0; s2 < kSlots; ++s2) mbar_init(&vready[s2], F8 ? 2 : 1);
     poison[1] = 0;
     *abort_flag = 0;
+    part_cnt[0] = part_cnt[1] = part_cnt[2] = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -1075,6 +1324,43 @@ __global__ void __launch_bounds__(384, 1)
               if ((vmask >> (grp + r)) & 1u) *reinterpret_cast<uint2 *>(dst0 + r * D + q * 32) = u[r];
           }
           if (valid) a.lse_part[slot_row] = lse_row;
+          if (a.unit_cnt != nullptr) {
+            // This warp's rows of the part are stored. The CTA's last warp to
+            // get here counts the part for the unit, and the CTA that counts
+            // a unit's last part merges the unit at the end of the pass.
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
+              int nvw = 0;  // warps of the CTA with rows in this part
+              for (int tt = 0; tt < sg.nt; ++tt)
+                for (int ww = 0; ww < 4; ++ww)
+                  nvw += (ww * 32 < a.rt && sg.pair * 2 * a.rt + tt * a.rt + ww * 32 < a.M) ? 1 : 0;
+              // only the range's first and last segments can be parts
+              const int k = sg.start + sg.lt0 == x0 ? 0 : 1;
+              if (atomicAdd(&part_cnt[k], 1) == nvw - 1) {
+                __threadfence();
+                const Owners own{total, static_cast<int64_t>(gridDim.x), a.owners32 != 0};
+                const int64_t c_first = own.of(sg.start), c_last = own.of(sg.start + sg.nkt - 1);
+                int parts = 0;
+                for (int64_t cc = c_first; cc <= c_last; ++cc) parts += own.owns(cc) ? 1 : 0;
+                if (atomicAdd(&a.unit_cnt[sg.unit], 1) == parts - 1) {
+                  __threadfence();
+                  const int e = atomicAdd(&part_cnt[2], 1);
+                  MergeEntry me;
+                  me.c_first = c_first;
+                  me.c_last = c_last;
+                  me.unit = static_cast<uint32_t>(sg.unit);
+                  me.pair = sg.pair;
+                  me.b = sg.b;
+                  me.hkv = sg.hkv;
+                  me.P = sg.P;
+                  me.pad = 0;
+                  mlist[e] = me;
+                }
+              }
+            }
+            __syncwarp();
+          }
         }
         tc_fence_before();
         mbar_arrive(&o_free[t]);
@@ -1092,6 +1378,34 @@ __global__ void __launch_bounds__(384, 1)
       named_arrive(p_bar_id(t, arrived), p_bar_threads(t));
       dts::report(a.err, DTS_DEV_TIMEOUT);
     }
+    if (a.unit_cnt != nullptr) {
+      // the units whose last part this CTA stored (at most two: only the
+      // range's first and last segments are parts), merged from every part,
+      // 8 rows per warp, once all eight softmax warps are past their last
+      // epilogue
+      named_sync(kMergeBarrier, 256);
+      if (*abort_flag == 0) {
+        MergeArgs ma{};
+        ma.o_part = a.o_part;
+        ma.lse_part = a.lse_part;
+        ma.out = a.out;
+        ma.lse2 = a.lse2;
+        ma.R = a.R;
+        ma.Hq = a.Hq;
+        ma.g = a.g;
+        ma.M = a.M;
+        ma.rt = a.rt;
+        ma.slot_rows = a.slot_rows;
+        const Owners own{total, static_cast<int64_t>(gridDim.x), a.owners32 != 0};
+        const int n = part_cnt[2];
+        const int rbs = (a.slot_rows + 7) / 8;
+        for (int e = 0; e < n; ++e) {
+          const MergeEntry me = mlist[e];
+          for (int rb = warp - 4; rb < rbs; rb += 8)
+            merge_rows<D, false>(ma, me.unit, rb, me.pair, me.b, me.hkv, me.P, me.c_first, me.c_last, own, lane);
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1099,98 +1413,6 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-}
-
-// ============================================================================
-// merge pass
-// ============================================================================
-struct MergeArgs {
-  const uint16_t *o_part;  // bf16 partial rows
-  const float *lse_part;
-  const int64_t *tiles_before;
-  const int32_t *prefix_len;
-  uint16_t *out;
-  float *lse2;
-  int64_t max_prefix, capacity;
-  int B, R, W, Hq, Hkv, g, M, rt, n_pairs, slot_rows, grid;  // W: window keys of the tree pass
-  int owners32;  // every (tile index + 1) * groups fits in 32 bits
-  // F8 only: the window part, from the bf16 rotated queries the prep pass
-  // left in `out`, the mask and the E4M3 window K/V in the paged cache
-  const uint64_t *mask;
-  const uint8_t *k8, *v8;
-  const int32_t *page_table;
-  int32_t *err;
-  int64_t num_slots;
-  int Ww, max_pages, page_shift;  // Ww: window keys of the window part
-  float scale_log2;
-};
-
-// Which group's range holds flat tile x, and whether group c owns any tile:
-// the tree pass gives group c the tiles [c T / G, (c + 1) T / G).
-struct Owners {
-  int64_t T, G;
-  bool w32;
-  __device__ int64_t of(int64_t x) const {  // ((x + 1) G - 1) / T
-    if (w32) return (static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(G) - 1u) / static_cast<uint32_t>(T);
-    return ((x + 1) * G - 1) / T;
-  }
-  __device__ bool owns(int64_t c) const {
-    if (w32) {
-      const uint32_t t = static_cast<uint32_t>(T), g = static_cast<uint32_t>(G), c32 = static_cast<uint32_t>(c);
-      return c32 * t / g < (c32 + 1u) * t / g;
-    }
-    return c * T / G < (c + 1) * T / G;
-  }
-};
-
-// F8 window part of one row: the row's visible window keys (bits of `bits`)
-// scored against its bf16 rotated query q[] (this lane's E columns) with the
-// E4M3 K rows widened exactly, an online softmax in base 2 (m, l) and the
-// unnormalised sum of the widened V rows in o[]. A non-finite K or V row
-// turns the rows that see it NaN. Returns false (after reporting) when a
-// window slot lies outside the cache; the row then reads NaN.
-template <int D>
-__device__ bool window_part_f8(const MergeArgs &a, int b, int hkv, int P, uint64_t bits, const float (&q)[D / 32],
-                               int lane, float &m, float &l, float (&o)[D / 32]) {
-  constexpr int E = D / 32;
-  static_assert(E == 4, "the E4M3 cache takes d = 128");
-  m = -INFINITY;
-  l = 0.f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) o[e] = 0.f;
-  const int ps = 1 << a.page_shift;
-  while (bits != 0ull) {
-    const int j = __ffsll(static_cast<long long>(bits)) - 1;
-    bits &= bits - 1ull;
-    const int pos = P + j;
-    const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
-    const int64_t slot = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
-    if (page < 0 || slot >= a.num_slots) {
-      if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
-      return false;
-    }
-    const int64_t off = (slot * a.Hkv + hkv) * D + E * lane;
-    const uint32_t kw = *reinterpret_cast<const uint32_t *>(a.k8 + off);
-    const uint32_t vw = *reinterpret_cast<const uint32_t *>(a.v8 + off);
-    const uint32_t k01 = dts::e4m3x2_to_f16x2(kw & 0xFFFFu), k23 = dts::e4m3x2_to_f16x2(kw >> 16);
-    const uint32_t v01 = dts::e4m3x2_to_f16x2(vw & 0xFFFFu), v23 = dts::e4m3x2_to_f16x2(vw >> 16);
-    const float k[4] = {dts::f16_lo(k01), dts::f16_hi(k01), dts::f16_lo(k23), dts::f16_hi(k23)};
-    const float v[4] = {dts::f16_lo(v01), dts::f16_hi(v01), dts::f16_lo(v23), dts::f16_hi(v23)};
-    float dot = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dot = fmaf(q[e], k[e], dot);
-#pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
-    const float sc = dot * a.scale_log2;
-    const float m_new = fmaxf(m, sc);  // (a NaN score leaves m; its weight below is NaN)
-    const float corr = m == -INFINITY ? 0.f : exp2f(m - m_new);
-    const float p = sc == -INFINITY ? 0.f : exp2f(sc - m_new);
-    l = l * corr + p;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = o[e] * corr + p * v[e];
-    m = m_new;
-  }
-  return true;
 }
 
 // One warp per 8 consecutive rows of a unit's slot (lane l holds columns
@@ -1207,7 +1429,6 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   dts::grid_dep_wait();
   dts::grid_dep_launch_next();
   constexpr int kRows = 8;
-  constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const uint32_t wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t blocks_per_unit = static_cast<uint32_t>((a.slot_rows + kRows - 1) / kRows);
@@ -1227,128 +1448,7 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   const int64_t start = pair * a.tiles_before[a.B] + a.tiles_before[b] + static_cast<int64_t>(hkv) * nkt;
   const int64_t c_first = nkt > 0 ? own.of(start) : 0, c_last = nkt > 0 ? own.of(start + nkt - 1) : -1;
   if (!F8 && c_first == c_last) return;  // one part: the tree pass wrote these rows
-
-  const int i_row = lane & 7;
-  const int prow_l = rb * kRows + i_row;
-  const bool row_ok = prow_l < a.slot_rows;
-  const int64_t row0 = static_cast<int64_t>(unit) * a.slot_rows + prow_l;  // this lane's row in slot `unit`
-
-  // pass 1: the largest LSE of each row (the first four parts' LSEs are kept)
-  float lse_first = -INFINITY;
-  float mx = -INFINITY;
-  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
-    const int64_t c = c0 + (lane >> 3);
-    float lse = -INFINITY;
-    if (c <= c_last && row_ok && own.owns(c)) lse = a.lse_part[row0 + c * a.slot_rows];
-    if (c0 == c_first) lse_first = lse;
-    mx = fmaxf(mx, lse);
-  }
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-  // pass 2: weights, their sum and the weighted rows
-  float acc[kRows][E];
-#pragma unroll
-  for (int i = 0; i < kRows; ++i)
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
-  float den = 0.f;
-  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
-    const int64_t c = c0 + (lane >> 3);
-    float lse = lse_first;
-    if (c0 != c_first) {
-      lse = -INFINITY;
-      if (c <= c_last && row_ok && own.owns(c)) lse = a.lse_part[row0 + c * a.slot_rows];
-    }
-    const float w = lse == -INFINITY ? 0.f : dts::ptx::ex2(lse - mx);  // a part that saw no key drops out
-    den += w;
-    // which of the four parts have rows to read (warp-uniform): a part whose
-    // weights are all 0 (not a group with tiles, or no key seen) is skipped
-    const uint32_t live = __ballot_sync(0xffffffffu, w != 0.f);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (((live >> (8 * k)) & 0xFFu) == 0u) continue;
-      const uint16_t *base =
-          a.o_part + ((static_cast<int64_t>(unit) + c0 + k) * a.slot_rows + rb * kRows) * D + E * lane;
-      float x[kRows][E];
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        if (rb * kRows + i < a.slot_rows) {
-          if constexpr (E == 4) {
-            const uint2 v = *reinterpret_cast<const uint2 *>(base + i * D);
-            x[i][0] = dts::bf16_lo(v.x);
-            x[i][1] = dts::bf16_hi(v.x);
-            x[i][2] = dts::bf16_lo(v.y);
-            x[i][3] = dts::bf16_hi(v.y);
-          } else {
-            const uint32_t v = *reinterpret_cast<const uint32_t *>(base + i * D);
-            x[i][0] = dts::bf16_lo(v);
-            x[i][1] = dts::bf16_hi(v);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < E; ++e) x[i][e] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        const float wi = __shfl_sync(0xffffffffu, w, k * 8 + i);
-        if (wi == 0.f) continue;  // warp-uniform
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[i][e] = fmaf(x[i][e], wi, acc[i][e]);
-      }
-    }
-  }
-  den += __shfl_xor_sync(0xffffffffu, den, 8);
-  den += __shfl_xor_sync(0xffffffffu, den, 16);
-
-#pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const int prow = rb * kRows + i;
-    float den_i = __shfl_sync(0xffffffffu, den, i);
-    float mx_i = __shfl_sync(0xffffffffu, mx, i);
-    const int R = pair * 2 * a.rt + prow;  // row of the KV head
-    if (prow >= a.slot_rows || R >= a.M) continue;
-    const int node = R / a.g;
-    const int64_t node_row = static_cast<int64_t>(b) * a.R + node;
-    const int64_t out_row = node_row * a.Hq + hkv * a.g + (R - node * a.g);
-    float num[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) num[e] = acc[i][e];
-    if constexpr (F8) {
-      // the window part: the prefix parts (lse mx_i, weight den_i) and the
-      // window keys (max m_w, weight l_w) meet at their common maximum
-      float q[E];
-      if constexpr (E == 4) {
-        const uint2 qw = *reinterpret_cast<const uint2 *>(a.out + out_row * D + E * lane);
-        q[0] = dts::bf16_lo(qw.x);
-        q[1] = dts::bf16_hi(qw.x);
-        q[2] = dts::bf16_lo(qw.y);
-        q[3] = dts::bf16_hi(qw.y);
-      }
-      const uint64_t bits = a.mask[node_row] & (a.Ww < 64 ? (1ull << a.Ww) - 1ull : ~0ull);
-      float m_w, l_w, o_w[E];
-      bool slot_ok = true;
-      if constexpr (E == 4) slot_ok = window_part_f8<D>(a, b, hkv, P, bits, q, lane, m_w, l_w, o_w);
-      const float M2 = fmaxf(mx_i, m_w);
-      const float ap = mx_i == -INFINITY ? 0.f : exp2f(mx_i - M2);
-      const float aw = m_w == -INFINITY ? 0.f : exp2f(m_w - M2);
-#pragma unroll
-      for (int e = 0; e < E; ++e) num[e] = ap * num[e] + aw * o_w[e];
-      den_i = ap * den_i + aw * l_w;
-      mx_i = M2;
-      if (!slot_ok) den_i = __int_as_float(0x7FC00000);
-    }
-    const float inv = den_i == 0.f ? 0.f : 1.f / den_i;  // (a NaN sum stays NaN)
-    if constexpr (E == 4) {
-      uint2 v;
-      v.x = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
-      v.y = dts::pack_bf16x2(num[2] * inv, num[3] * inv);
-      *reinterpret_cast<uint2 *>(a.out + out_row * D + E * lane) = v;
-    } else {
-      *reinterpret_cast<uint32_t *>(a.out + out_row * D + E * lane) = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
-    }
-    if (lane == 0) a.lse2[out_row] = den_i == 0.f ? -INFINITY : mx_i + __log2f(den_i);
-  }
+  merge_rows<D, F8>(a, unit, rb, pair, b, hkv, P, c_first, c_last, own, lane);
 }
 
 // ============================================================================
@@ -1472,11 +1572,25 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   uint16_t *o_part = reinterpret_cast<uint16_t *>(ws + plan.o_off);
   float *lse_part = reinterpret_cast<float *>(ws + plan.lse_off);
   int64_t *tiles_before = reinterpret_cast<int64_t *>(ws + plan.tb_off);
+  int32_t *unit_cnt = reinterpret_cast<int32_t *>(ws + plan.cnt_off);
   uint16_t *q_rot = reinterpret_cast<uint16_t *>(ws + plan.q_off);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf(static_cast<float>(d));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int page_shift = __builtin_ctz(static_cast<unsigned>(page_size));
   const int g = Hq / Hkv;
+
+  // Units of at most 128 rows split over CTAs are merged by the tree pass
+  // itself (the CTA that stores a unit's last part, with its eight softmax
+  // warps) when every CTA has many key tiles: such a merge is short against
+  // the pass, and the merge launch is saved. Larger units (several parts of
+  // 256 rows) go to the merge pass, which spreads them over the whole GPU; so
+  // do short passes, where the merge would lengthen the last CTAs, and every
+  // unit under F8, whose window keys the merge pass adds.
+  const int sms = dts_host::sm_count();
+  const int grid = sms > 0 ? (sms < kMaxGrid ? sms : kMaxGrid) : 1;
+  const int64_t tiles_bound =
+      static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + (f8 ? 0 : W) + 127) / 128);
+  const bool merge_in_pass = !f8 && plan.slot_rows <= 128 && tiles_bound >= 64ll * grid;
 
   // 0. prep: rotated queries, NaN rows for bad prefix lengths
   {
@@ -1496,6 +1610,8 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
     ra.Hq = Hq;
     ra.heads_per_thread = (Hq % 4 == 0) ? 4 : (Hq % 2 == 0) ? 2 : 1;
     ra.to_e4m3 = f8 ? 1 : 0;
+    ra.unit_cnt = merge_in_pass ? unit_cnt : nullptr;
+    ra.units = plan.units;
     if (positions != nullptr) dts_host::make_rope_freqs(rope_theta, d, &ra.freqs);
     const int64_t items = static_cast<int64_t>(B) * R * (Hq / ra.heads_per_thread) * (d / 16);
     const int blocks = static_cast<int>((items + 255) / 256);
@@ -1506,8 +1622,6 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   const uint16_t *q_eff = (positions != nullptr || f8) ? q_rot : q;
 
   // 1. tree attention, one CTA per SM
-  const int sms = dts_host::sm_count();
-  const int grid = sms > 0 ? (sms < kMaxGrid ? sms : kMaxGrid) : 1;
   CUtensorMap tk, tv, tq;
   const int rpb = page_size < 128 ? page_size : 128;
   if (!make_cache_map(&tk, k_cache, d, Hkv, num_slots, rpb, f8) ||
@@ -1542,12 +1656,22 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   pa.scale_log2 = scale * kLog2e;
   pa.wait_budget = g_test_wait_budget.load(std::memory_order_relaxed);
   pa.stall = g_test_stall.load(std::memory_order_relaxed);
+  pa.unit_cnt = merge_in_pass ? unit_cnt : nullptr;
+  int owners32 = 0;
+  {
+    // the largest possible tile total, times the groups, against 2^32
+    const int64_t max_tiles = static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + pa.W + 127) / 128);
+    owners32 = static_cast<double>(max_tiles + 1) * grid < 4294967296.0 ? 1 : 0;
+  }
+  pa.owners32 = owners32;
   const int st = f8          ? launch_prefix<128, true>(tk, tv, tq, pa, grid, s)
                  : d == 128 ? launch_prefix<128, false>(tk, tv, tq, pa, grid, s)
                             : launch_prefix<64, false>(tk, tv, tq, pa, grid, s);
   if (st != DTS_OK) return st;
+  if (merge_in_pass) return DTS_OK;
 
-  // 2. merge pass: units whose key tiles went to more than one CTA
+  // 2. merge pass: units whose key tiles went to more than one CTA (F8:
+  // every unit, with its rows' window keys)
   MergeArgs ma;
   ma.o_part = o_part;
   ma.lse_part = lse_part;
@@ -1578,11 +1702,7 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   ma.n_pairs = plan.n_pairs;
   ma.slot_rows = plan.slot_rows;
   ma.grid = grid;
-  {
-    // the largest possible tile total, times the groups, against 2^32
-    const int64_t max_tiles = static_cast<int64_t>(B) * Hkv * plan.n_pairs * ((max_prefix + pa.W + 127) / 128);
-    ma.owners32 = static_cast<double>(max_tiles + 1) * grid < 4294967296.0 ? 1 : 0;
-  }
+  ma.owners32 = owners32;
   const int64_t warps = plan.units * ((plan.slot_rows + 7) / 8);
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   if (f8) dts_host::launch_chained(tree_merge_kernel<128, true>, dim3(blocks), dim3(256), 0, s, ma);

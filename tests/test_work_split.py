@@ -91,3 +91,48 @@ def test_two_row_pairs_walk_in_mirror():
         first = {(sg["cta"], sg["key"][1:], sg["lt0"], sg["lt1"]) for sg in segs if sg["key"][0] == 0}
         second = {(sg["cta"] - G // 2, sg["key"][1:], sg["lt0"], sg["lt1"]) for sg in segs if sg["key"][0] == 1}
         assert first == second
+
+
+def test_split_units_merge_once_in_the_pass():
+    """Without FP8 the tree pass merges a unit split over CTAs itself: every
+    CTA holding a part counts it once (per-CTA counters 0 and 1 for its
+    range's first and last segments, the only ones that can be parts), and
+    the CTA that brings a unit's count to its number of parts (the groups
+    c_first .. c_last that own tiles) merges it. The model checks that each
+    split unit's parts are exactly those CTAs, that no CTA has more than two
+    parts or two parts on one counter, and that in any arrival order exactly
+    one CTA merges each split unit."""
+    rng = random.Random(13)
+    for _ in range(300):
+        B = rng.randint(1, 40)
+        prefix = [rng.choice([0, 1, 127, 128, 500, 4096, 8192, rng.randint(0, 20000)]) for _ in range(B)]
+        Hkv = rng.choice([1, 2, 8])
+        n_pairs = rng.choice([1, 1, 2, 3])
+        G = rng.choice([1, 7, 152])
+        units, starts, T, segs = _segments(prefix, Hkv, n_pairs, G)
+        parts_of = {}
+        per_cta = {}
+        for sg in segs:
+            u = units[sg["unit"]]
+            if sg["lt0"] == 0 and sg["lt1"] == u[3]:
+                continue  # a whole unit: written by its CTA, no part
+            x0 = T * sg["cta"] // G
+            k = 0 if starts[sg["unit"]] + sg["lt0"] == x0 else 1
+            per_cta.setdefault(sg["cta"], []).append(k)
+            parts_of.setdefault(sg["unit"], []).append(sg["cta"])
+        for c, ks in per_cta.items():
+            assert len(ks) <= 2 and len(set(ks)) == len(ks), (c, ks)
+        for ui, ctas in parts_of.items():
+            s0, nkt = starts[ui], units[ui][3]
+            c0, c1 = _owner(s0, T, G), _owner(s0 + nkt - 1, T, G)
+            parts = sum(1 for c in range(c0, c1 + 1) if T * c // G < T * (c + 1) // G)
+            assert sorted(ctas) == list(range(c0, c1 + 1)) or len(ctas) == parts
+            assert len(ctas) == parts >= 2
+            order = ctas[:]
+            rng.shuffle(order)
+            cnt, mergers = 0, []
+            for c in order:
+                if cnt == parts - 1:
+                    mergers.append(c)
+                cnt += 1
+            assert len(mergers) == 1
