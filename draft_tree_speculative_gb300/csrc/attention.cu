@@ -288,12 +288,18 @@ __device__ bool window_part_f8(const MergeArgs &a, int b, int hkv, int P, uint64
 
 // The merge of rows [8 rb, 8 rb + 8) of unit `unit` (row pair `pair`, request
 // b, KV head hkv, prefix length P) by one warp, from the parts left by the
-// groups c_first .. c_last of the tree pass.
-template <int D, bool F8>
+// groups c_first .. c_last of the tree pass. kInPass: called by the tree pass
+// itself, whose other CTAs stored the parts during the pass: their loads go to
+// L2, past this SM's L1.
+template <int D, bool F8, bool kInPass = false>
 __device__ __forceinline__ void merge_rows(const MergeArgs &a, uint32_t unit, int rb, int pair, int b, int hkv, int P,
                                            int64_t c_first, int64_t c_last, const Owners &own, int lane) {
   constexpr int kRows = 8;
   constexpr int E = D / 32;
+  auto ld_part = [](const auto *p) {
+    if constexpr (kInPass) return __ldcg(p);
+    else return *p;
+  };
   const int i_row = lane & 7;
   const int prow_l = rb * kRows + i_row;
   const bool row_ok = prow_l < a.slot_rows;
@@ -305,7 +311,7 @@ __device__ __forceinline__ void merge_rows(const MergeArgs &a, uint32_t unit, in
   for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
     const int64_t c = c0 + (lane >> 3);
     float lse = -INFINITY;
-    if (c <= c_last && row_ok && own.owns(c)) lse = __ldcg(a.lse_part + row0 + c * a.slot_rows);
+    if (c <= c_last && row_ok && own.owns(c)) lse = ld_part(a.lse_part + row0 + c * a.slot_rows);
     if (c0 == c_first) lse_first = lse;
     mx = fmaxf(mx, lse);
   }
@@ -323,7 +329,7 @@ __device__ __forceinline__ void merge_rows(const MergeArgs &a, uint32_t unit, in
     float lse = lse_first;
     if (c0 != c_first) {
       lse = -INFINITY;
-      if (c <= c_last && row_ok && own.owns(c)) lse = __ldcg(a.lse_part + row0 + c * a.slot_rows);
+      if (c <= c_last && row_ok && own.owns(c)) lse = ld_part(a.lse_part + row0 + c * a.slot_rows);
     }
     const float w = lse == -INFINITY ? 0.f : dts::ptx::ex2(lse - mx);  // a part that saw no key drops out
     den += w;
@@ -340,13 +346,13 @@ __device__ __forceinline__ void merge_rows(const MergeArgs &a, uint32_t unit, in
       for (int i = 0; i < kRows; ++i) {
         if (rb * kRows + i < a.slot_rows) {
           if constexpr (E == 4) {
-            const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(base + i * D));
+            const uint2 v = ld_part(reinterpret_cast<const uint2 *>(base + i * D));
             x[i][0] = dts::bf16_lo(v.x);
             x[i][1] = dts::bf16_hi(v.x);
             x[i][2] = dts::bf16_lo(v.y);
             x[i][3] = dts::bf16_hi(v.y);
           } else {
-            const uint32_t v = __ldcg(reinterpret_cast<const unsigned int *>(base + i * D));
+            const uint32_t v = ld_part(reinterpret_cast<const unsigned int *>(base + i * D));
             x[i][0] = dts::bf16_lo(v);
             x[i][1] = dts::bf16_hi(v);
           }
@@ -1324,7 +1330,7 @@ __global__ void __launch_bounds__(384, 1)
               if ((vmask >> (grp + r)) & 1u) *reinterpret_cast<uint2 *>(dst0 + r * D + q * 32) = u[r];
           }
           if (valid) a.lse_part[slot_row] = lse_row;
-          if (a.unit_cnt != nullptr) {
+          if (!F8 && a.unit_cnt != nullptr) {
             // This warp's rows of the part are stored. The CTA's last warp to
             // get here counts the part for the unit, and the CTA that counts
             // a unit's last part merges the unit at the end of the pass.
@@ -1378,7 +1384,7 @@ __global__ void __launch_bounds__(384, 1)
       named_arrive(p_bar_id(t, arrived), p_bar_threads(t));
       dts::report(a.err, DTS_DEV_TIMEOUT);
     }
-    if (a.unit_cnt != nullptr) {
+    if (!F8 && a.unit_cnt != nullptr) {
       // the units whose last part this CTA stored (at most two: only the
       // range's first and last segments are parts), merged from every part,
       // 8 rows per warp, once all eight softmax warps are past their last
@@ -1402,7 +1408,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int e = 0; e < n; ++e) {
           const MergeEntry me = mlist[e];
           for (int rb = warp - 4; rb < rbs; rb += 8)
-            merge_rows<D, false>(ma, me.unit, rb, me.pair, me.b, me.hkv, me.P, me.c_first, me.c_last, own, lane);
+            merge_rows<D, false, true>(ma, me.unit, rb, me.pair, me.b, me.hkv, me.P, me.c_first, me.c_last, own,
+                                       lane);
         }
       }
     }
