@@ -114,6 +114,14 @@ EDGE = [
     ("g8_two_row_pairs", "longctx_p131072_n64", dict(B=2, prefix=[700, 2050]), None),
     ("g2", "llama8b_p4096_n8", dict(B=2, Hq=16, Hkv=8, prefix=[1500, 10]), None),
     ("g16", "llama8b_p4096_n8", dict(B=2, Hq=32, Hkv=2, prefix=[900, 33]), "random"),
+    # 64-row units on a long pass: split units are merged inside the tree
+    # pass; tile-edge, ragged and long prefixes side by side. (No empty
+    # prefixes here: a row that sees only its few window keys can move its LSE
+    # by ~1.5e-3 when one rotated query or key element rounds to the other
+    # neighbouring bf16 value than the exact rotation does, which the window
+    # write test bounds by one ulp; the short-prefix cases above cover them.)
+    ("in_pass_merge_ragged", "highconc_b128_n16",
+     dict(B=128, prefix=[64, 127, 128, 129, 700, 2049, 4000, 300] * 16), "random"),
 ]
 
 
