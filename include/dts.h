@@ -180,7 +180,10 @@ size_t dts_tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d,
  * puts the window past max_pages * page_size gets NaN rows and
  * DTS_DEV_BAD_SLOT; so does a page id outside the pool.
  * Launches three kernels on `stream` (query rotation, the tensor-core pass
- * over prefix and window keys, the merge of units split over CTAs).
+ * over prefix and window keys, the merge of units split over CTAs), or two
+ * when the tensor-core pass merges the split units itself (units of at most
+ * 128 query rows on a long pass). The kernels are chained by programmatic
+ * dependent launch, each waiting for its predecessor before it reads memory.
  */
 int dts_tree_verify_attention(const uint16_t *q, const uint16_t *k_cache,
                               const uint16_t *v_cache, int64_t num_slots,
