@@ -236,54 +236,192 @@ struct Owners {
   }
 };
 
-// F8 window part of one row: the row's visible window keys (bits of `bits`)
-// scored against its bf16 rotated query q[] (this lane's E columns) with the
-// E4M3 K rows widened exactly, an online softmax in base 2 (m, l) and the
-// unnormalised sum of the widened V rows in o[]. A non-finite K or V row
-// turns the rows that see it NaN. Returns false (after reporting) when a
-// window slot lies outside the cache; the row then reads NaN.
-template <int D>
-__device__ bool window_part_f8(const MergeArgs &a, int b, int hkv, int P, uint64_t bits, const float (&q)[D / 32],
-                               int lane, float &m, float &l, float (&o)[D / 32]) {
-  constexpr int E = D / 32;
-  static_assert(E == 4, "the E4M3 cache takes d = 128");
-  m = -INFINITY;
-  l = 0.f;
+// The F8 merge of rows [8 rb, 8 rb + 8) of unit `unit` by one warp. Lane
+// 4 r + c holds row r's columns {32 t + 8 c + u : t < 4, u < 8}. Each row
+// first takes its visible window keys against its bf16 rotated query (left in
+// `out` by the prep pass), with the E4M3 K and V rows widened exactly, in an
+// online softmax in base 2 (m, l, o). The warp walks the union of its rows'
+// visible keys once: every key's K and V rows are loaded once for all eight
+// rows, two keys at a time, and each row takes only the keys its mask holds.
+// The prefix parts of the tree pass then join at the common maximum M:
+// O = (2^(m - M) o + sum_k 2^(lse_k - M) O_k) / (2^(m - M) l + sum_k 2^(lse_k
+// - M)), lse = M + log2 of that denominator. A non-finite K or V row turns
+// the rows that see it NaN; a row whose window slot lies outside the cache
+// reads NaN (after reporting).
+__device__ __forceinline__ void merge_rows_f8(const MergeArgs &a, uint32_t unit, int rb, int pair, int b, int hkv,
+                                              int P, int64_t c_first, int64_t c_last, const Owners &own, int lane) {
+  constexpr int D = 128;
+  const int r = lane >> 2, c = lane & 3;
+  const int prow = rb * 8 + r;
+  const int R = pair * 2 * a.rt + prow;  // row of the KV head
+  const bool row_ok = prow < a.slot_rows;
+  const bool valid = row_ok && R < a.M;
+  const int node = valid ? R / a.g : 0;
+  const int64_t node_row = static_cast<int64_t>(b) * a.R + node;
+  const int64_t out_row = node_row * a.Hq + hkv * a.g + (R - node * a.g);
+  const int64_t part_row = static_cast<int64_t>(unit) * a.slot_rows + prow;  // + part * slot_rows
+
+  uint4 qv[4];
 #pragma unroll
-  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  for (int t = 0; t < 4; ++t)
+    qv[t] = valid ? *reinterpret_cast<const uint4 *>(a.out + out_row * D + 32 * t + 8 * c) : make_uint4(0, 0, 0, 0);
+  const uint64_t bits = valid ? a.mask[node_row] & (a.Ww < 64 ? (1ull << a.Ww) - 1ull : ~0ull) : 0ull;
+
+  // pass 1: the largest LSE of the row's parts (lane c takes parts c, c + 4, ...;
+  // the first four parts' LSEs are kept)
+  float lse_first = -INFINITY, mx = -INFINITY;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    const int64_t part = c0 + c;
+    float lse = -INFINITY;
+    if (part <= c_last && row_ok && own.owns(part)) lse = a.lse_part[part_row + part * a.slot_rows];
+    if (c0 == c_first) lse_first = lse;
+    mx = fmaxf(mx, lse);
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+
+  // the window keys any of the eight rows sees; lane l looks up the slots of
+  // keys l and l + 32
+  uint64_t uni = bits;
+  uni |= __shfl_xor_sync(0xffffffffu, uni, 4);
+  uni |= __shfl_xor_sync(0xffffffffu, uni, 8);
+  uni |= __shfl_xor_sync(0xffffffffu, uni, 16);
   const int ps = 1 << a.page_shift;
-  while (bits != 0ull) {
-    const int j = __ffsll(static_cast<long long>(bits)) - 1;
-    bits &= bits - 1ull;
-    const int pos = P + j;
+  int64_t slot_lo = 0, slot_hi = 0;
+  bool bad_lo = false, bad_hi = false;
+  if ((uni >> lane) & 1ull) {
+    const int pos = P + lane;
     const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
-    const int64_t slot = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
-    if (page < 0 || slot >= a.num_slots) {
-      if (lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
-      return false;
-    }
-    const int64_t off = (slot * a.Hkv + hkv) * D + E * lane;
-    const uint32_t kw = *reinterpret_cast<const uint32_t *>(a.k8 + off);
-    const uint32_t vw = *reinterpret_cast<const uint32_t *>(a.v8 + off);
-    const uint32_t k01 = dts::e4m3x2_to_f16x2(kw & 0xFFFFu), k23 = dts::e4m3x2_to_f16x2(kw >> 16);
-    const uint32_t v01 = dts::e4m3x2_to_f16x2(vw & 0xFFFFu), v23 = dts::e4m3x2_to_f16x2(vw >> 16);
-    const float k[4] = {dts::f16_lo(k01), dts::f16_hi(k01), dts::f16_lo(k23), dts::f16_hi(k23)};
-    const float v[4] = {dts::f16_lo(v01), dts::f16_hi(v01), dts::f16_lo(v23), dts::f16_hi(v23)};
+    slot_lo = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
+    bad_lo = page < 0 || slot_lo >= a.num_slots;
+  }
+  if ((uni >> (lane + 32)) & 1ull) {
+    const int pos = P + lane + 32;
+    const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
+    slot_hi = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
+    bad_hi = page < 0 || slot_hi >= a.num_slots;
+  }
+  const uint64_t bad = static_cast<uint64_t>(__ballot_sync(0xffffffffu, bad_lo)) |
+                       (static_cast<uint64_t>(__ballot_sync(0xffffffffu, bad_hi)) << 32);
+  if (bad != 0ull && lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
+
+  float m = -INFINITY, l = 0.f, o[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o[i] = 0.f;
+  // one key j (K and V words kw, vw of this lane's columns) for the rows that see it
+  auto take_key = [&](int j, const uint2 (&kw)[4], const uint2 (&vw)[4]) {
     float dot = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) dot = fmaf(q[e], k[e], dot);
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t k01 = dts::e4m3x2_to_f16x2(kw[t].x & 0xFFFFu), k23 = dts::e4m3x2_to_f16x2(kw[t].x >> 16);
+      const uint32_t k45 = dts::e4m3x2_to_f16x2(kw[t].y & 0xFFFFu), k67 = dts::e4m3x2_to_f16x2(kw[t].y >> 16);
+      dot = fmaf(dts::bf16_lo(qv[t].x), dts::f16_lo(k01), dot);
+      dot = fmaf(dts::bf16_hi(qv[t].x), dts::f16_hi(k01), dot);
+      dot = fmaf(dts::bf16_lo(qv[t].y), dts::f16_lo(k23), dot);
+      dot = fmaf(dts::bf16_hi(qv[t].y), dts::f16_hi(k23), dot);
+      dot = fmaf(dts::bf16_lo(qv[t].z), dts::f16_lo(k45), dot);
+      dot = fmaf(dts::bf16_hi(qv[t].z), dts::f16_hi(k45), dot);
+      dot = fmaf(dts::bf16_lo(qv[t].w), dts::f16_lo(k67), dot);
+      dot = fmaf(dts::bf16_hi(qv[t].w), dts::f16_hi(k67), dot);
+    }
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    if ((bits >> j) & 1ull) {
+      const float sc = dot * a.scale_log2;
+      const float m_new = fmaxf(m, sc);  // (a NaN score leaves m; its weight below is NaN)
+      const float corr = m == -INFINITY ? 0.f : exp2f(m - m_new);
+      const float p = sc == -INFINITY ? 0.f : exp2f(sc - m_new);
+      l = l * corr + p;
 #pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
-    const float sc = dot * a.scale_log2;
-    const float m_new = fmaxf(m, sc);  // (a NaN score leaves m; its weight below is NaN)
-    const float corr = m == -INFINITY ? 0.f : exp2f(m - m_new);
-    const float p = sc == -INFINITY ? 0.f : exp2f(sc - m_new);
-    l = l * corr + p;
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t v01 = dts::e4m3x2_to_f16x2(vw[t].x & 0xFFFFu), v23 = dts::e4m3x2_to_f16x2(vw[t].x >> 16);
+        const uint32_t v45 = dts::e4m3x2_to_f16x2(vw[t].y & 0xFFFFu), v67 = dts::e4m3x2_to_f16x2(vw[t].y >> 16);
+        const float v[8] = {dts::f16_lo(v01), dts::f16_hi(v01), dts::f16_lo(v23), dts::f16_hi(v23),
+                            dts::f16_lo(v45), dts::f16_hi(v45), dts::f16_lo(v67), dts::f16_hi(v67)};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = o[e] * corr + p * v[e];
-    m = m_new;
+        for (int u = 0; u < 8; ++u) o[8 * t + u] = o[8 * t + u] * corr + p * v[u];
+      }
+      m = m_new;
+    }
+  };
+  uint64_t todo = uni & ~bad;
+  while (todo != 0ull) {
+    const int j0 = __ffsll(static_cast<long long>(todo)) - 1;
+    todo &= todo - 1ull;
+    const int j1 = todo != 0ull ? __ffsll(static_cast<long long>(todo)) - 1 : -1;
+    if (j1 >= 0) todo &= todo - 1ull;
+    const int64_t s0 = __shfl_sync(0xffffffffu, j0 < 32 ? slot_lo : slot_hi, j0 & 31);
+    const int64_t s1 = __shfl_sync(0xffffffffu, j1 < 32 ? slot_lo : slot_hi, j1 & 31);
+    uint2 k0[4], v0[4], k1[4], v1[4];
+    const int64_t off0 = (s0 * a.Hkv + hkv) * D + 8 * c, off1 = (s1 * a.Hkv + hkv) * D + 8 * c;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      k0[t] = *reinterpret_cast<const uint2 *>(a.k8 + off0 + 32 * t);
+      v0[t] = *reinterpret_cast<const uint2 *>(a.v8 + off0 + 32 * t);
+    }
+    if (j1 >= 0) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        k1[t] = *reinterpret_cast<const uint2 *>(a.k8 + off1 + 32 * t);
+        v1[t] = *reinterpret_cast<const uint2 *>(a.v8 + off1 + 32 * t);
+      }
+    }
+    take_key(j0, k0, v0);
+    if (j1 >= 0) take_key(j1, k1, v1);
   }
-  return true;
+
+  // pass 2: the window sum and the parts at the common maximum
+  const float M2 = fmaxf(mx, m);
+  const float aw = m == -INFINITY ? 0.f : exp2f(m - M2);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o[i] *= aw;
+  float den_parts = 0.f;  // this lane's parts (c, c + 4, ...)
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    float lse = lse_first;
+    if (c0 != c_first) {
+      const int64_t part = c0 + c;
+      lse = -INFINITY;
+      if (part <= c_last && row_ok && own.owns(part)) lse = a.lse_part[part_row + part * a.slot_rows];
+    }
+    const float w = lse == -INFINITY ? 0.f : dts::ptx::ex2(lse - M2);  // a part that saw no key drops out
+    den_parts += w;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (c0 + k > c_last) break;
+      const float wk = __shfl_sync(0xffffffffu, w, (lane & ~3) | k);
+      if (wk != 0.f) {
+        const uint16_t *src = a.o_part + (part_row + (c0 + k) * a.slot_rows) * D + 8 * c;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(src + 32 * t);
+          o[8 * t + 0] = fmaf(dts::bf16_lo(x.x), wk, o[8 * t + 0]);
+          o[8 * t + 1] = fmaf(dts::bf16_hi(x.x), wk, o[8 * t + 1]);
+          o[8 * t + 2] = fmaf(dts::bf16_lo(x.y), wk, o[8 * t + 2]);
+          o[8 * t + 3] = fmaf(dts::bf16_hi(x.y), wk, o[8 * t + 3]);
+          o[8 * t + 4] = fmaf(dts::bf16_lo(x.z), wk, o[8 * t + 4]);
+          o[8 * t + 5] = fmaf(dts::bf16_hi(x.z), wk, o[8 * t + 5]);
+          o[8 * t + 6] = fmaf(dts::bf16_lo(x.w), wk, o[8 * t + 6]);
+          o[8 * t + 7] = fmaf(dts::bf16_hi(x.w), wk, o[8 * t + 7]);
+        }
+      }
+    }
+  }
+  den_parts += __shfl_xor_sync(0xffffffffu, den_parts, 1);
+  den_parts += __shfl_xor_sync(0xffffffffu, den_parts, 2);
+  float den = aw * l + den_parts;  // (a NaN window sum stays NaN)
+  if ((bits & bad) != 0ull) den = __int_as_float(0x7FC00000);
+  if (!valid) return;
+  const float inv = den == 0.f ? 0.f : 1.f / den;  // (a NaN sum stays NaN)
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    uint4 y;
+    y.x = dts::pack_bf16x2(o[8 * t + 0] * inv, o[8 * t + 1] * inv);
+    y.y = dts::pack_bf16x2(o[8 * t + 2] * inv, o[8 * t + 3] * inv);
+    y.z = dts::pack_bf16x2(o[8 * t + 4] * inv, o[8 * t + 5] * inv);
+    y.w = dts::pack_bf16x2(o[8 * t + 6] * inv, o[8 * t + 7] * inv);
+    *reinterpret_cast<uint4 *>(a.out + out_row * D + 32 * t + 8 * c) = y;
+  }
+  if (c == 0) a.lse2[out_row] = den == 0.f ? -INFINITY : M2 + __log2f(den);
 }
 
 // The merge of rows [8 rb, 8 rb + 8) of unit `unit` (row pair `pair`, request
@@ -291,7 +429,7 @@ __device__ bool window_part_f8(const MergeArgs &a, int b, int hkv, int P, uint64
 // groups c_first .. c_last of the tree pass. kInPass: called by the tree pass
 // itself, whose other CTAs stored the parts during the pass: their loads go to
 // L2, past this SM's L1.
-template <int D, bool F8, bool kInPass = false>
+template <int D, bool kInPass = false>
 __device__ __forceinline__ void merge_rows(const MergeArgs &a, uint32_t unit, int rb, int pair, int b, int hkv, int P,
                                            int64_t c_first, int64_t c_last, const Owners &own, int lane) {
   constexpr int kRows = 8;
@@ -376,48 +514,22 @@ __device__ __forceinline__ void merge_rows(const MergeArgs &a, uint32_t unit, in
 #pragma unroll
   for (int i = 0; i < kRows; ++i) {
     const int prow = rb * kRows + i;
-    float den_i = __shfl_sync(0xffffffffu, den, i);
-    float mx_i = __shfl_sync(0xffffffffu, mx, i);
+    const float den_i = __shfl_sync(0xffffffffu, den, i);
+    const float mx_i = __shfl_sync(0xffffffffu, mx, i);
     const int R = pair * 2 * a.rt + prow;  // row of the KV head
     if (prow >= a.slot_rows || R >= a.M) continue;
     const int node = R / a.g;
     const int64_t node_row = static_cast<int64_t>(b) * a.R + node;
     const int64_t out_row = node_row * a.Hq + hkv * a.g + (R - node * a.g);
-    float num[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) num[e] = acc[i][e];
-    if constexpr (F8) {
-      // the window part: the prefix parts (lse mx_i, weight den_i) and the
-      // window keys (max m_w, weight l_w) meet at their common maximum
-      float q[E];
-      if constexpr (E == 4) {
-        const uint2 qw = *reinterpret_cast<const uint2 *>(a.out + out_row * D + E * lane);
-        q[0] = dts::bf16_lo(qw.x);
-        q[1] = dts::bf16_hi(qw.x);
-        q[2] = dts::bf16_lo(qw.y);
-        q[3] = dts::bf16_hi(qw.y);
-      }
-      const uint64_t bits = a.mask[node_row] & (a.Ww < 64 ? (1ull << a.Ww) - 1ull : ~0ull);
-      float m_w, l_w, o_w[E];
-      bool slot_ok = true;
-      if constexpr (E == 4) slot_ok = window_part_f8<D>(a, b, hkv, P, bits, q, lane, m_w, l_w, o_w);
-      const float M2 = fmaxf(mx_i, m_w);
-      const float ap = mx_i == -INFINITY ? 0.f : exp2f(mx_i - M2);
-      const float aw = m_w == -INFINITY ? 0.f : exp2f(m_w - M2);
-#pragma unroll
-      for (int e = 0; e < E; ++e) num[e] = ap * num[e] + aw * o_w[e];
-      den_i = ap * den_i + aw * l_w;
-      mx_i = M2;
-      if (!slot_ok) den_i = __int_as_float(0x7FC00000);
-    }
     const float inv = den_i == 0.f ? 0.f : 1.f / den_i;  // (a NaN sum stays NaN)
     if constexpr (E == 4) {
       uint2 v;
-      v.x = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
-      v.y = dts::pack_bf16x2(num[2] * inv, num[3] * inv);
+      v.x = dts::pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
+      v.y = dts::pack_bf16x2(acc[i][2] * inv, acc[i][3] * inv);
       *reinterpret_cast<uint2 *>(a.out + out_row * D + E * lane) = v;
     } else {
-      *reinterpret_cast<uint32_t *>(a.out + out_row * D + E * lane) = dts::pack_bf16x2(num[0] * inv, num[1] * inv);
+      *reinterpret_cast<uint32_t *>(a.out + out_row * D + E * lane) =
+          dts::pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
     }
     if (lane == 0) a.lse2[out_row] = den_i == 0.f ? -INFINITY : mx_i + __log2f(den_i);
   }
@@ -1408,7 +1520,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int e = 0; e < n; ++e) {
           const MergeEntry me = mlist[e];
           for (int rb = warp - 4; rb < rbs; rb += 8)
-            merge_rows<D, false, true>(ma, me.unit, rb, me.pair, me.b, me.hkv, me.P, me.c_first, me.c_last, own,
+            merge_rows<D, true>(ma, me.unit, rb, me.pair, me.b, me.hkv, me.P, me.c_first, me.c_last, own,
                                        lane);
         }
       }
@@ -1422,15 +1534,15 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// One warp per 8 consecutive rows of a unit's slot (lane l holds columns
-// [E l, E l + E), E = d/32). Without F8 a unit whose key tiles all fell to
-// one CTA was written by the tree pass; the others merge their parts'
-// partial rows by their LSEs: O = sum_k 2^(lse_k - m) O_k / sum_k 2^(lse_k -
-// m), lse = m + log2(sum_k 2^(lse_k - m)), m the largest lse_k. Under F8
-// every unit comes here, its parts cover the prefix only, and the window
-// part (window_part_f8) joins the sum as one more part.
-// Parts go four at a time: lane = part * 8 + row reads one LSE and decides
-// once whether its group owns tiles; the row loads of the four parts follow.
+// One warp per 8 consecutive rows of a unit's slot. Without F8 (lane l holds
+// columns [E l, E l + E), E = d/32) a unit whose key tiles all fell to one
+// CTA was written by the tree pass; the others merge their parts' partial
+// rows by their LSEs: O = sum_k 2^(lse_k - m) O_k / sum_k 2^(lse_k - m), lse
+// = m + log2(sum_k 2^(lse_k - m)), m the largest lse_k. Parts go four at a
+// time: lane = part * 8 + row reads one LSE and decides once whether its
+// group owns tiles; the row loads of the four parts follow. Under F8 every
+// unit comes here, its parts cover the prefix only, and merge_rows_f8 adds
+// the rows' window keys as one more part.
 template <int D, bool F8>
 __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__ MergeArgs a) {
   dts::grid_dep_wait();
@@ -1455,7 +1567,8 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   const int64_t start = pair * a.tiles_before[a.B] + a.tiles_before[b] + static_cast<int64_t>(hkv) * nkt;
   const int64_t c_first = nkt > 0 ? own.of(start) : 0, c_last = nkt > 0 ? own.of(start + nkt - 1) : -1;
   if (!F8 && c_first == c_last) return;  // one part: the tree pass wrote these rows
-  merge_rows<D, F8>(a, unit, rb, pair, b, hkv, P, c_first, c_last, own, lane);
+  if constexpr (F8) merge_rows_f8(a, unit, rb, pair, b, hkv, P, c_first, c_last, own, lane);
+  else merge_rows<D>(a, unit, rb, pair, b, hkv, P, c_first, c_last, own, lane);
 }
 
 // ============================================================================
