@@ -236,23 +236,27 @@ struct Owners {
   }
 };
 
-// The F8 merge of rows [8 rb, 8 rb + 8) of unit `unit` by one warp. Lane
-// 4 r + c holds row r's columns {32 t + 8 c + u : t < 4, u < 8}. Each row
-// first takes its visible window keys against its bf16 rotated query (left in
-// `out` by the prep pass), with the E4M3 K and V rows widened exactly, in an
-// online softmax in base 2 (m, l, o). The warp walks the union of its rows'
-// visible keys once: every key's K and V rows are loaded once for all eight
-// rows, two keys at a time, and each row takes only the keys its mask holds.
-// The prefix parts of the tree pass then join at the common maximum M:
-// O = (2^(m - M) o + sum_k 2^(lse_k - M) O_k) / (2^(m - M) l + sum_k 2^(lse_k
-// - M)), lse = M + log2 of that denominator. A non-finite K or V row turns
-// the rows that see it NaN; a row whose window slot lies outside the cache
-// reads NaN (after reporting).
-__device__ __forceinline__ void merge_rows_f8(const MergeArgs &a, uint32_t unit, int rb, int pair, int b, int hkv,
-                                              int P, int64_t c_first, int64_t c_last, const Owners &own, int lane) {
+// The F8 merge of rows [64 blk, 64 blk + 64) of unit `unit` (row pair `pair`,
+// request b, KV head hkv, prefix length P) by one CTA of eight warps, warp w
+// taking 8 rows; lane 4 r + c of a warp holds its row r's columns
+// {32 t + 8 c + u : t < 4, u < 8}. Each row first takes its visible window
+// keys against its bf16 rotated query (left in `out` by the prep pass), with
+// the E4M3 K and V rows widened exactly, in an online softmax in base 2
+// (m, l, o). The window's K and V rows are copied into shared memory once
+// for the CTA; a warp walks the union of its rows' visible keys, each row
+// taking only the keys its mask holds. The prefix parts of the tree pass
+// then join at the common maximum M: O = (2^(m - M) o + sum_k 2^(lse_k - M)
+// O_k) / (2^(m - M) l + sum_k 2^(lse_k - M)), lse = M + log2 of that
+// denominator. A non-finite K or V row turns the rows that see it NaN; a row
+// whose window slot lies outside the cache reads NaN (after reporting).
+__device__ __forceinline__ void merge_block_f8(const MergeArgs &a, uint32_t unit, int blk, int pair, int b, int hkv,
+                                               int P, int64_t c_first, int64_t c_last, const Owners &own) {
   constexpr int D = 128;
+  __shared__ __align__(128) uint8_t kv_s[2][dts::kMaxNodes * D];  // E4M3 window K | V rows
+  __shared__ uint32_t bad_s[2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, c = lane & 3;
-  const int prow = rb * 8 + r;
+  const int prow = (blk * 8 + warp) * 8 + r;
   const int R = pair * 2 * a.rt + prow;  // row of the KV head
   const bool row_ok = prow < a.slot_rows;
   const bool valid = row_ok && R < a.M;
@@ -277,44 +281,55 @@ __device__ __forceinline__ void merge_rows_f8(const MergeArgs &a, uint32_t unit,
     if (c0 == c_first) lse_first = lse;
     mx = fmaxf(mx, lse);
   }
+
+  // the window's K and V rows into shared memory: warps 0 and 1 take keys
+  // 32 w + lane, whose slots they look up and check
+  if (warp < 2) {
+    const int j = 32 * warp + lane;
+    bool bad = false;
+    if (j < a.Ww) {
+      const int pos = P + j;
+      const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
+      const int64_t slot = (static_cast<int64_t>(page) << a.page_shift) + (pos & ((1 << a.page_shift) - 1));
+      bad = page < 0 || slot >= a.num_slots;
+      if (!bad) {
+        const int64_t off = (slot * a.Hkv + hkv) * D;
+#pragma unroll
+        for (int x = 0; x < D / 16; ++x) {
+          dts::ptx::cp_async_16(&kv_s[0][j * D + 16 * x], a.k8 + off + 16 * x);
+          dts::ptx::cp_async_16(&kv_s[1][j * D + 16 * x], a.v8 + off + 16 * x);
+        }
+      }
+    }
+    const uint32_t bw = __ballot_sync(0xffffffffu, bad);
+    if (lane == 0) bad_s[warp] = bw;
+    dts::ptx::cp_async_wait_all();
+  }
+  __syncthreads();
+  if (!__any_sync(0xffffffffu, row_ok)) return;  // a warp past the slot's rows
+  const uint64_t bad = a.Ww > 32 ? bad_s[0] | (static_cast<uint64_t>(bad_s[1]) << 32) : bad_s[0];
+
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-
-  // the window keys any of the eight rows sees; lane l looks up the slots of
-  // keys l and l + 32
-  uint64_t uni = bits;
+  uint64_t uni = bits;  // the window keys any of the warp's eight rows sees
   uni |= __shfl_xor_sync(0xffffffffu, uni, 4);
   uni |= __shfl_xor_sync(0xffffffffu, uni, 8);
   uni |= __shfl_xor_sync(0xffffffffu, uni, 16);
-  const int ps = 1 << a.page_shift;
-  int64_t slot_lo = 0, slot_hi = 0;
-  bool bad_lo = false, bad_hi = false;
-  if ((uni >> lane) & 1ull) {
-    const int pos = P + lane;
-    const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
-    slot_lo = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
-    bad_lo = page < 0 || slot_lo >= a.num_slots;
-  }
-  if ((uni >> (lane + 32)) & 1ull) {
-    const int pos = P + lane + 32;
-    const int page = a.page_table[static_cast<int64_t>(b) * a.max_pages + (pos >> a.page_shift)];
-    slot_hi = static_cast<int64_t>(page) * ps + (pos & (ps - 1));
-    bad_hi = page < 0 || slot_hi >= a.num_slots;
-  }
-  const uint64_t bad = static_cast<uint64_t>(__ballot_sync(0xffffffffu, bad_lo)) |
-                       (static_cast<uint64_t>(__ballot_sync(0xffffffffu, bad_hi)) << 32);
-  if (bad != 0ull && lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
+  if ((uni & bad) != 0ull && lane == 0) dts::report(a.err, DTS_DEV_BAD_SLOT);
 
   float m = -INFINITY, l = 0.f, o[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) o[i] = 0.f;
-  // one key j (K and V words kw, vw of this lane's columns) for the rows that see it
-  auto take_key = [&](int j, const uint2 (&kw)[4], const uint2 (&vw)[4]) {
+  uint64_t todo = uni & ~bad;
+  while (todo != 0ull) {
+    const int j = __ffsll(static_cast<long long>(todo)) - 1;
+    todo &= todo - 1ull;
     float dot = 0.f;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t k01 = dts::e4m3x2_to_f16x2(kw[t].x & 0xFFFFu), k23 = dts::e4m3x2_to_f16x2(kw[t].x >> 16);
-      const uint32_t k45 = dts::e4m3x2_to_f16x2(kw[t].y & 0xFFFFu), k67 = dts::e4m3x2_to_f16x2(kw[t].y >> 16);
+      const uint2 kw = *reinterpret_cast<const uint2 *>(&kv_s[0][j * D + 32 * t + 8 * c]);
+      const uint32_t k01 = dts::e4m3x2_to_f16x2(kw.x & 0xFFFFu), k23 = dts::e4m3x2_to_f16x2(kw.x >> 16);
+      const uint32_t k45 = dts::e4m3x2_to_f16x2(kw.y & 0xFFFFu), k67 = dts::e4m3x2_to_f16x2(kw.y >> 16);
       dot = fmaf(dts::bf16_lo(qv[t].x), dts::f16_lo(k01), dot);
       dot = fmaf(dts::bf16_hi(qv[t].x), dts::f16_hi(k01), dot);
       dot = fmaf(dts::bf16_lo(qv[t].y), dts::f16_lo(k23), dot);
@@ -334,8 +349,9 @@ __device__ __forceinline__ void merge_rows_f8(const MergeArgs &a, uint32_t unit,
       l = l * corr + p;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const uint32_t v01 = dts::e4m3x2_to_f16x2(vw[t].x & 0xFFFFu), v23 = dts::e4m3x2_to_f16x2(vw[t].x >> 16);
-        const uint32_t v45 = dts::e4m3x2_to_f16x2(vw[t].y & 0xFFFFu), v67 = dts::e4m3x2_to_f16x2(vw[t].y >> 16);
+        const uint2 vw = *reinterpret_cast<const uint2 *>(&kv_s[1][j * D + 32 * t + 8 * c]);
+        const uint32_t v01 = dts::e4m3x2_to_f16x2(vw.x & 0xFFFFu), v23 = dts::e4m3x2_to_f16x2(vw.x >> 16);
+        const uint32_t v45 = dts::e4m3x2_to_f16x2(vw.y & 0xFFFFu), v67 = dts::e4m3x2_to_f16x2(vw.y >> 16);
         const float v[8] = {dts::f16_lo(v01), dts::f16_hi(v01), dts::f16_lo(v23), dts::f16_hi(v23),
                             dts::f16_lo(v45), dts::f16_hi(v45), dts::f16_lo(v67), dts::f16_hi(v67)};
 #pragma unroll
@@ -343,31 +359,6 @@ __device__ __forceinline__ void merge_rows_f8(const MergeArgs &a, uint32_t unit,
       }
       m = m_new;
     }
-  };
-  uint64_t todo = uni & ~bad;
-  while (todo != 0ull) {
-    const int j0 = __ffsll(static_cast<long long>(todo)) - 1;
-    todo &= todo - 1ull;
-    const int j1 = todo != 0ull ? __ffsll(static_cast<long long>(todo)) - 1 : -1;
-    if (j1 >= 0) todo &= todo - 1ull;
-    const int64_t s0 = __shfl_sync(0xffffffffu, j0 < 32 ? slot_lo : slot_hi, j0 & 31);
-    const int64_t s1 = __shfl_sync(0xffffffffu, j1 < 32 ? slot_lo : slot_hi, j1 & 31);
-    uint2 k0[4], v0[4], k1[4], v1[4];
-    const int64_t off0 = (s0 * a.Hkv + hkv) * D + 8 * c, off1 = (s1 * a.Hkv + hkv) * D + 8 * c;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      k0[t] = *reinterpret_cast<const uint2 *>(a.k8 + off0 + 32 * t);
-      v0[t] = *reinterpret_cast<const uint2 *>(a.v8 + off0 + 32 * t);
-    }
-    if (j1 >= 0) {
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        k1[t] = *reinterpret_cast<const uint2 *>(a.k8 + off1 + 32 * t);
-        v1[t] = *reinterpret_cast<const uint2 *>(a.v8 + off1 + 32 * t);
-      }
-    }
-    take_key(j0, k0, v0);
-    if (j1 >= 0) take_key(j1, k1, v1);
   }
 
   // pass 2: the window sum and the parts at the common maximum
@@ -1534,22 +1525,22 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// One warp per 8 consecutive rows of a unit's slot. Without F8 (lane l holds
-// columns [E l, E l + E), E = d/32) a unit whose key tiles all fell to one
+// Without F8, one warp per 8 consecutive rows of a unit's slot (lane l holds
+// columns [E l, E l + E), E = d/32): a unit whose key tiles all fell to one
 // CTA was written by the tree pass; the others merge their parts' partial
 // rows by their LSEs: O = sum_k 2^(lse_k - m) O_k / sum_k 2^(lse_k - m), lse
 // = m + log2(sum_k 2^(lse_k - m)), m the largest lse_k. Parts go four at a
 // time: lane = part * 8 + row reads one LSE and decides once whether its
 // group owns tiles; the row loads of the four parts follow. Under F8 every
-// unit comes here, its parts cover the prefix only, and merge_rows_f8 adds
-// the rows' window keys as one more part.
+// unit comes here, one CTA per 64 rows of its slot: its parts cover the
+// prefix only, and merge_block_f8 adds the rows' window keys as one more part.
 template <int D, bool F8>
 __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__ MergeArgs a) {
   dts::grid_dep_wait();
   dts::grid_dep_launch_next();
-  constexpr int kRows = 8;
+  constexpr int kRows = F8 ? 64 : 8;  // rows of a CTA (F8) or of a warp
   const int lane = threadIdx.x & 31;
-  const uint32_t wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t wid = F8 ? blockIdx.x : (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t blocks_per_unit = static_cast<uint32_t>((a.slot_rows + kRows - 1) / kRows);
   const uint32_t unit = wid / blocks_per_unit;
   // units in the flat order of the tree pass: (row pair, request, KV head)
@@ -1566,9 +1557,12 @@ __global__ void __launch_bounds__(256) tree_merge_kernel(const __grid_constant__
   const Owners own{a.tiles_before[a.B] * a.n_pairs, a.grid, a.owners32 != 0};
   const int64_t start = pair * a.tiles_before[a.B] + a.tiles_before[b] + static_cast<int64_t>(hkv) * nkt;
   const int64_t c_first = nkt > 0 ? own.of(start) : 0, c_last = nkt > 0 ? own.of(start + nkt - 1) : -1;
-  if (!F8 && c_first == c_last) return;  // one part: the tree pass wrote these rows
-  if constexpr (F8) merge_rows_f8(a, unit, rb, pair, b, hkv, P, c_first, c_last, own, lane);
-  else merge_rows<D>(a, unit, rb, pair, b, hkv, P, c_first, c_last, own, lane);
+  if constexpr (F8) {
+    merge_block_f8(a, unit, rb, pair, b, hkv, P, c_first, c_last, own);
+  } else {
+    if (c_first == c_last) return;  // one part: the tree pass wrote these rows
+    merge_rows<D>(a, unit, rb, pair, b, hkv, P, c_first, c_last, own, lane);
+  }
 }
 
 // ============================================================================
@@ -1823,8 +1817,10 @@ int window_attention(bool f8, const uint16_t *q, const void *k_cache, const void
   ma.slot_rows = plan.slot_rows;
   ma.grid = grid;
   ma.owners32 = owners32;
+  // (F8: one CTA of 256 threads per 64 rows of a unit; else one warp per 8 rows)
   const int64_t warps = plan.units * ((plan.slot_rows + 7) / 8);
-  const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+  const int blocks = f8 ? static_cast<int>(plan.units * ((plan.slot_rows + 63) / 64))
+                        : static_cast<int>((warps * 32 + 255) / 256);
   if (f8) dts_host::launch_chained(tree_merge_kernel<128, true>, dim3(blocks), dim3(256), 0, s, ma);
   else if (d == 128) dts_host::launch_chained(tree_merge_kernel<128, false>, dim3(blocks), dim3(256), 0, s, ma);
   else dts_host::launch_chained(tree_merge_kernel<64, false>, dim3(blocks), dim3(256), 0, s, ma);
