@@ -52,10 +52,10 @@ def _verify_case(w, trees=None):
     return inp, k8, v8
 
 
-def _run_verify_fp8(inp, k8, v8, rotate=True):
+def _run_verify_fp8(inp, k8, v8, rotate=True, page_table=None, expect_err=0):
     """GPU: the tree's masks and positions (build_tree_mask), then the
     attention with the query rotated at each node's position (or taken as
-    already rotated)."""
+    already rotated); the device error code must read `expect_err`."""
     torch = torch_cuda()
     w, lay = inp.w, inp.layout
     B, N = w.B, w.N
@@ -69,11 +69,12 @@ def _run_verify_fp8(inp, k8, v8, rotate=True):
     max_prefix = int(lay.prefix_len.max())
     ws = torch.empty(dts.tree_verify_attention_workspace(B, N, w.Hq, w.Hkv, w.d, max_prefix), dtype=torch.uint8,
                      device="cuda")
-    dts.tree_verify_attention_fp8(_bf(inp.q), _dev(k8), _dev(v8), _dev(lay.page_table), w.page_size,
+    pt = lay.page_table if page_table is None else page_table
+    dts.tree_verify_attention_fp8(_bf(inp.q), _dev(k8), _dev(v8), _dev(pt), w.page_size,
                                   _dev(lay.prefix_len), max_prefix, mask, pos if rotate else None, w.rope_theta, out,
                                   lse, ws, err=err)
     torch.cuda.synchronize()
-    assert int(err.item()) == 0
+    assert int(err.item()) == expect_err
     return bf16_to_f64(out), lse.cpu().numpy().astype(np.float64)
 
 
@@ -178,6 +179,33 @@ def test_verify_fp8_nan_bytes_reach_only_the_rows_that_see_them():
     for b in range(w.B):
         assert not np.isfinite(out[b * N + leaf]).all()
     assert np.array_equal(out[keep], out_ref[keep])
+
+
+def test_verify_fp8_bad_window_page_reaches_only_the_rows_that_see_it():
+    """A window page id that points outside the cache (-1 for request 0's
+    last window page, past the cache for request 1's) is reported as a bad
+    slot and turns exactly the rows that see one of its keys NaN: with pages
+    of 16 keys and depth-first numbering those are nodes 48..63. Every other
+    row still matches the oracle. The prefixes end on a key-tile edge, so no
+    prefix tile reaches the broken pages."""
+    w = custom_workload("eagle2_p8192_n64", 64, B=2, prefix=[1024, 640], Hq=8, page_size=16)
+    rng = np.random.default_rng(640)
+    par = np.stack([random_tree(rng, w.N)[0] for _ in range(w.B)]).astype(np.int32)
+    dep = np.stack([synth.depth_of(p) for p in par]).astype(np.int32)
+    inp, k8, v8 = _verify_case(w, trees=(par, dep))
+    lay, N, ps = inp.layout, w.N, w.page_size
+    pt = lay.page_table.copy()
+    num_pages = lay.num_slots // ps
+    for b, bad in ((0, -1), (1, num_pages + 5)):
+        last = (int(lay.prefix_len[b]) + N - 1) // ps
+        assert last == (int(lay.prefix_len[b]) + 48) // ps          # keys 48..63 share the last page
+        pt[b, last] = bad
+    out, lse = _run_verify_fp8(inp, k8, v8, page_table=pt, expect_err=dts.DEV_BAD_SLOT)
+    hit = [b * N + i for b in range(w.B) for i in range(48, N)]
+    keep = [r for r in range(w.B * N) if r not in hit]
+    rows, ro, rl = _oracle_verify_fp8(inp, k8, v8, range(w.B))
+    assert_attention_close(out[keep], lse[keep], ro[keep], rl[keep], range(len(keep)))
+    assert np.isnan(out[hit]).all() and np.isnan(lse[hit]).all()
 
 
 # ---------------------------------------------------------------------------- draft lanes (R = K, W = (S-1) K)
