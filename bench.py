@@ -749,7 +749,8 @@ def time_fp8_attention(inp, db, stream, flush, args, hbm, tf_sus):
     roof["hbm_frac"] = t_hbm / t
     roof["traffic_tree_pass"] = recorded_traffic("fp8:" + w.name)
     return {"workload": w.name, "kv_dtype": "e4m3 (unscaled)",
-            "compute": "S: E4M3 MMA (query cast to E4M3); P V: f16 MMA (V widened); fp32 accumulation",
+            "compute": ("prefix keys: E4M3 S MMA (query cast to E4M3), f16 P V MMA (V widened), fp32 accumulation; "
+                        "window keys: bf16 query against exactly widened E4M3 K/V in fp32; parts merged by LSE"),
             "us": us, "rows_per_s": BN / t, "bytes": nbytes, "flops": flops, "roofline": roof, "reps": reps}
 
 

@@ -262,15 +262,17 @@ int dts_tree_window_attention(const uint16_t *q, const uint16_t *k_cache,
  * dts_tree_window_attention / dts_tree_verify_attention over E4M3 caches
  * [num_slots][Hkv][d] (bytes, 16-byte aligned), with the same workspace
  * sizes (dts_tree_window_attention_workspace /
- * dts_tree_verify_attention_workspace). The query (rotated and rounded to
- * bf16 as for the bf16 cache, or as given when positions is NULL) is cast to
- * E4M3 as the prefix decode over an FP8 cache does, and every key, prefix or
- * window, is scored against that query: S = Q K^T is one E4M3 tensor-core
- * product with fp32 accumulation. V is widened to f16 (exact), the softmax
- * weights enter P.V as f16, accumulation is fp32. d = 128 only
- * (DTS_ERR_UNSUPPORTED otherwise); every other argument, output rule and error
- * is that of the bf16 call, a NaN byte in a window key's V row standing for
- * the non-finite V row there.
+ * dts_tree_verify_attention_workspace). The query is rotated and rounded to
+ * bf16 as for the bf16 cache (or taken as given when positions is NULL). The
+ * prefix keys [0, P) are scored against that query cast to E4M3, as the
+ * prefix decode over an FP8 cache does: S = Q K^T is one E4M3 tensor-core
+ * product with fp32 accumulation, V is widened to f16 (exact), the softmax
+ * weights enter P.V as f16 and accumulate in fp32. The window keys [P, P + W)
+ * are scored against the unquantized bf16 query, with their K and V rows
+ * widened exactly from E4M3 and fp32 arithmetic; the two parts then merge by
+ * their log-sum-exps. d = 128 only (DTS_ERR_UNSUPPORTED otherwise); every
+ * other argument, output rule and error is that of the bf16 call, a NaN byte
+ * in a window key's V row standing for the non-finite V row there.
  */
 int dts_write_window_kv_fp8(const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
                             const int32_t *page_table, int max_pages, int page_size,
